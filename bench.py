@@ -1,0 +1,482 @@
+"""Benchmark: paged decode attention over a tree-shaped KV cache on one GB300.
+
+Default workload: ``long_context`` -- 64 q-heads / 8 kv-heads, head_dim 128,
+bf16, block 16; 128 sequences of 8192 tokens plus 16 roots of 32768 tokens
+each forked into 16 branches of 512 suffix tokens (6.98 GB of unique KV, far
+larger than L2, so no L2 flush is needed between steps).  One step = one
+``paged_decode_attn`` call: every kernel of the decode step (split-KV pass,
+shared-prefix pass when tensor-core tiles exist, LSE merge) for all 384
+branches.
+
+Metric: unique-KV GB/s (distinct physical blocks read in the step x the valid
+tokens of each x Hkv x d x 2 bytes x 2 for K and V, divided by the step
+time); branch-queries/s is reported beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-cpu-baseline]
+
+``--impl reference`` times the fp64 CPU oracle on the host cores (the only
+reference implementation that exists for this path) on a bounded sample of
+the same workload.  Under torchrun (N > 1) each rank runs an independent
+replica of the workload (the path does not shard across GPUs): no collective
+on the data path; the barrier and max-over-ranks timing stay.
+"""
+
+from __future__ import annotations
+
+import os
+
+# The oracle baseline parallelises over query rows with threads; keep BLAS to
+# one thread per worker so "cores" is the number of threads really used.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import concurrent.futures as cf  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn: unique-KV GB/s vs HBM peak; branch-queries/sec"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long_context")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            low = line.lower()
+            if low.startswith("model name") or low.startswith("cpu part"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def unique_kv_bytes(tables, seq_lens, Hkv, d):
+    """Distinct physical blocks read in the step, each weighted by the valid
+    tokens in it, times Hkv * d * 2 bytes * 2 (K and V)."""
+    valid = {}
+    for row, L in zip(tables, seq_lens):
+        nblk = (int(L) + 15) // 16
+        for j in range(nblk):
+            n = min(16, int(L) - 16 * j)
+            b = int(row[j])
+            valid[b] = max(valid.get(b, 0), n)
+    return sum(valid.values()) * Hkv * d * 2 * 2
+
+
+def item_bytes(plan, info, Hkv, d, seq_lens, which):
+    """Algorithmic KV bytes one launch of a kernel reads: for each of its work
+    items, the valid tokens of its block range x 2 (K, V) x d x 2 bytes."""
+    off = 16 if which == "row" else 16 + 8 * info.n_row_items
+    n = info.n_row_items if which == "row" else info.n_tile_items
+    items = plan[off:off + 8 * n].reshape(-1, 8)
+    tot = 0
+    for b0, g, row0, nr, lo, hi, pb, masked in items:
+        toks = (hi - lo) * 16
+        if masked:
+            toks = min(toks, int(seq_lens[b0]) - 16 * lo)
+        tot += toks
+    return tot * 2 * d * 2
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_per_launch(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(f"{kernel}/{workload}")
+    if not d:
+        return None
+    src = os.path.join(ROOT, "paged_kv_cache_attn_gb300", "csrc", d["source"])
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return d["dram_bytes_per_launch"] if sha == d["source_sha"] else None
+
+
+# ---- the oracle as the CPU baseline ----------------------------------------------
+
+def prepare_sample(w, max_rows):
+    """Pick up to max_rows batch rows (spread over the batch so every kind of
+    branch is in it) and materialise their contiguous K/V and queries on the
+    host.  Not timed: this is input preparation, not the oracle's work."""
+    from oracle import replay as rp
+    ref = rp.replay(w, with_data=False)
+    nb = len(ref.decode_ids)
+    q = w.queries(nb)
+    rows = sorted(set(np.linspace(0, nb - 1, min(max_rows, nb)).astype(int)
+                      .tolist()))
+    sample = []
+    for b in rows:
+        k, v = ref.branch_kv(ref.decode_ids[b])
+        sample.append((q[b], k[0], v[0]))
+    return sample, nb
+
+
+def oracle_unit(w, item, g):
+    """The oracle on one (branch, kv-head): its G query heads against all of
+    the branch's tokens.  Returns the KV bytes it read."""
+    from oracle import attention as att
+    qb, K, V = item
+    G = w.Hq // w.Hkv
+    att.attention(att.bf16_to_f64(qb[g * G:(g + 1) * G]),
+                  att.bf16_to_f64(K[:, g]), att.bf16_to_f64(V[:, g]), w.scale)
+    return K.shape[0] * w.d * 2 * 2
+
+
+def run_units(w, sample, units, cores, ex):
+    parts = [units[j::cores] for j in range(cores) if units[j::cores]]
+
+    def part(us):
+        return sum(oracle_unit(w, sample[i], g) for i, g in us)
+
+    return sum(f.result() for f in [ex.submit(part, p) for p in parts])
+
+
+def cpu_baseline(w, budget_s=15.0):
+    """Oracle throughput on host threads over a bounded sample of the batch."""
+    sample, nb = prepare_sample(w, 24)
+    units = [(i, g) for i in range(len(sample)) for g in range(w.Hkv)]
+    cores = min(host_cores(), len(units))
+    done, byts, t0 = 0, 0, time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        while done < len(units) and time.perf_counter() - t0 < budget_s:
+            chunk = units[done:done + cores]
+            byts += run_units(w, sample, chunk, cores, ex)
+            done += len(chunk)
+    dt = time.perf_counter() - t0
+    return {"value": round(byts / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{done} (branch, kv-head) units from {len(sample)} of "
+                      f"{nb} branches of {w.name} ({byts / 1e9:.2f} GB of KV), "
+                      f"fp64 numpy, {dt:.1f} s wall",
+            "cpu": cpu_model()}
+
+
+# ---- our arm ------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    from paged_kv_cache_attn_gb300 import binding as B
+    from paged_kv_cache_attn_gb300 import harness as H
+    from paged_kv_cache_attn_gb300 import workloads as W
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = f"cuda:{local if ws > 1 else 0}"
+    torch.cuda.set_device(dev)
+    w = W.CONFIGS[args.workload]()
+    cache = H.Cache(w, device=dev)
+    bt = cache.batch().upload()
+    nb = bt.nb
+    q_host = w.queries(nb)
+    q = torch.from_numpy(q_host.view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.empty_like(q)
+    uniq = unique_kv_bytes(bt.tables, bt.seq_lens, w.Hkv, w.d)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(args.warmup, 3)):
+        bt.decode(q, out)
+    torch.cuda.synchronize()
+    code, detail = bt.device_status()
+    if code:
+        raise RuntimeError(f"device status {code} ({detail})")
+
+    # Timed region: K steps, per-kernel events recorded by the library.
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)]
+           for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        start.record(stream)
+        for i in range(K):
+            B.kv_set_launch_events(evs[i])
+            bt.decode(q, out)
+        end.record(stream)
+        B.kv_set_launch_events(None)
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    ms = start.elapsed_time(end)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / K
+    per_kernel = {}
+    names = ["tile_tcgen05", "splitkv_mma", "lse_merge"]
+    for k, name in enumerate(names):
+        if k == 0 and bt.info.n_tile_items == 0:
+            continue
+        if k == 1 and bt.info.n_row_items == 0:
+            continue
+        per_kernel[name] = sum(e[2 * k].elapsed_time(e[2 * k + 1])
+                               for e in evs) / K
+    code, detail = bt.device_status()
+    if code:
+        raise RuntimeError(f"device status {code} ({detail})")
+    launches_per_step = len(per_kernel)
+
+    # Dominant kernel and its roofline.
+    dom = max((k for k in per_kernel if k != "lse_merge"),
+              key=lambda k: per_kernel[k])
+    alg = item_bytes(bt.plan, bt.info, w.Hkv, w.d, bt.seq_lens,
+                     "row" if dom == "splitkv_mma" else "tile")
+    peak, peak_kind = measured_peaks()
+    achieved = alg / (per_kernel[dom] / 1e3) / 1e9
+    kname = {"splitkv_mma": "splitkv_decode_kernel",
+             "tile_tcgen05": "tile_decode_kernel"}[dom]
+    traffic = traffic_per_launch(kname, w.name)
+
+    # End to end through the public API with host buffers: per step, build the
+    # batch and plan on the host, copy q / tables / lengths / segments / plan
+    # host -> device from pinned memory, run the step, copy out back.
+    q_pin = torch.from_numpy(q_host.view(np.int16)).pin_memory()
+    out_pin = torch.empty((nb, w.Hq, w.d), dtype=torch.int16).pin_memory()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    e2e_t, h2d, d2h = [], 0, 0
+    for i in range(args.e2e_steps + 3):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        tables, lens, groups = B.kv_build_batch(cache.h, bt.ids)
+        plan, info = B.paged_decode_plan(nb, w.Hq, w.Hkv, w.d,
+                                         tables.shape[1], lens, groups, sms)
+        host = [torch.from_numpy(a).pin_memory() for a in
+                (tables, lens, groups.reshape(-1) if len(groups)
+                 else np.zeros(4, np.int32), plan)]
+        devs = [x.to(dev, non_blocking=True) for x in host]
+        qd = q_pin.to(dev, non_blocking=True).view(torch.bfloat16)
+        wsb = bt.dev["workspace"]
+        if wsb.numel() < info.workspace_bytes:
+            wsb = torch.empty(info.workspace_bytes, dtype=torch.uint8, device=dev)
+        B.paged_decode_attn(qd, cache.k[0], cache.v[0], w.num_blocks, devs[0],
+                            devs[1], devs[2], len(groups), nb, tables.shape[1],
+                            w.Hq, w.Hkv, w.d, w.scale, out, devs[3], info, wsb,
+                            wsb.numel())
+        out_pin.copy_(out.view(torch.int16), non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= 3:
+            e2e_t.append(time.perf_counter() - t0)
+        h2d = sum(x.numel() * x.element_size() for x in host) + \
+            q_pin.numel() * q_pin.element_size()
+        d2h = out_pin.numel() * out_pin.element_size()
+    e2e_s = statistics.median(e2e_t)
+
+    res = None
+    if rank == 0:
+        clocks = clk.summary()
+        res = {
+            "metric": METRIC,
+            "value": round(uniq * ws / (ms_step / 1e3) / 1e9, 1),
+            "unit": "GB/s",
+            "n_gpus": ws,
+            "steps": K,
+            "warmup": max(args.warmup, 3),
+            "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "branch_queries_per_s": round(nb * ws / (ms_step / 1e3), 1),
+            "config": {
+                "workload": w.name,
+                "description": w.description,
+                "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d, "block_size": 16,
+                "branches": nb,
+                "unique_kv_bytes": uniq,
+                "segments": int(len(bt.groups)),
+                "l2": "inputs larger than L2 (unique KV far above 129 MB); "
+                      "no flush",
+                "parallelism": f"replicas x{ws}",
+            },
+            "kernels_ms": {k: round(v, 5) for k, v in per_kernel.items()},
+            "roofline": {
+                "kernel": kname,
+                "bound": "hbm",
+                "achieved": round(achieved, 1),
+                "peak": peak,
+                "peak_kind": peak_kind,
+                "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": traffic,
+                "algorithmic_bytes_per_launch": alg,
+            },
+            "e2e": {
+                "value": round(uniq / e2e_s / 1e9, 1),
+                "unit": "GB/s",
+                "ms_per_step": round(e2e_s * 1e3, 4),
+                "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h),
+            },
+            "gpu_launches": launches_per_step * K,
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline and ws == 1:
+            res["cpu_baseline"] = cpu_baseline(w)
+    if ws > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    cache.close()
+    return res
+
+
+def run_reference(args):
+    """The fp64 oracle on host threads; each step one bounded sample."""
+    from paged_kv_cache_attn_gb300 import workloads as W
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    w = W.CONFIGS[args.workload]()
+    sample, nb = prepare_sample(w, 16)
+    units = [(i, g) for i in range(len(sample)) for g in range(w.Hkv)]
+    np.random.default_rng(3).shuffle(units)
+    cores = min(host_cores(), len(units))
+    # Size a step so the whole run takes about two minutes.
+    t0 = time.perf_counter()
+    oracle_unit(w, sample[units[0][0]], units[0][1])
+    unit_s = max(time.perf_counter() - t0, 1e-4)
+    per_step = 120.0 / (args.steps + args.warmup)
+    per = max(1, min(len(units), int(per_step * cores / unit_s)))
+    times, byts, pos = [], [], 0
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        for i in range(args.warmup + args.steps):
+            chunk = [units[(pos + j) % len(units)] for j in range(per)]
+            pos += per
+            t0 = time.perf_counter()
+            b = run_units(w, sample, chunk, min(cores, per), ex)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+                byts.append(b)
+    total_t = sum(times)
+    val = sum(byts) / total_t / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(val, 4),
+        "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_t / len(times) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description},
+        "cpu_baseline": {"value": round(val, 4), "unit": "GB/s",
+                         "cores": min(cores, per), "kind": "oracle",
+                         "sample": f"{per} (branch, kv-head) units per step "
+                                   f"from {len(sample)} of {nb} branches of "
+                                   f"{w.name}, fp64 numpy",
+                         "cpu": cpu_model()},
+        "e2e": {"value": round(val, 4), "unit": "GB/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,626 @@
+// Decode attention over the paged pool: the split-KV kernel, the log-sum-exp
+// merge, and the paged_decode_attn entry point.
+//
+// What is computed ("The Reasoning Engine Meltdown", §2.1): for each branch b
+// and q-head h, softmax(scale * q K^T) V over the branch's cached tokens,
+// token t read from block table[b][t / 16], slot t % 16 ("Dismantling the
+// Memory Wall", PagedAttention section), kv-head h / (Hq / Hkv).
+//
+// Split-KV kernel (one CTA = one work item = up to 16 query rows x one
+// kv-head x a range of logical blocks):
+//  * 4 warps; warp w takes blocks w, w + 4, ... of the range.  Each warp runs
+//    its own NS-stage ring: lane 0 issues two 2-D TMA loads per 64 columns of
+//    the (block, kv-head) K and V tiles (16 rows x 128 B, 128-byte swizzle)
+//    completing on the stage's mbarrier; the whole warp waits on it.
+//  * S = Q K^T with mma.sync m16n8k16: query rows are M (16), the block's
+//    16 tokens are N (two n8 tiles), head_dim is K.  The S accumulator layout
+//    is the A-operand layout of the next product, so P never leaves
+//    registers: O += P V with V read by ldmatrix.trans.
+//  * Online softmax in base 2 (scores pre-multiplied by scale * log2(e)),
+//    row maxima and sums reduced across the four lanes of a row with
+//    shuffles.
+//  * The four warps' (m, l, O) are combined through shared memory and written
+//    as one unnormalised partial row per query row.
+// The merge kernel combines each (branch, q-head)'s partial rows:
+// m* = max m_i, l* = sum l_i 2^(m_i - m*), out = sum o_i 2^(m_i - m*) / l*.
+
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "device_common.cuh"
+
+namespace pkv {
+
+struct SplitParams {
+  const __nv_bfloat16* q;
+  const int32_t* tables;
+  const int32_t* seq_lens;
+  const WorkItem* items;
+  float2* ml;
+  float* o;
+  DeviceStatus* status;
+  int nb, Hq, Hkv, G, max_blocks;
+  int64_t num_blocks;
+  int64_t partial_rows;
+  float scale_log2;
+};
+
+// A work item read from the (caller-uploaded) plan must stay inside the
+// arrays it indexes; a malformed one is recorded and skipped.
+__device__ __forceinline__ bool item_ok(const WorkItem& it,
+                                        const SplitParams& p, int max_rows) {
+  const int64_t last_row = (int64_t)it.row0 + it.nrows - 1;
+  return it.nrows >= 1 && it.nrows <= max_rows && it.row0 >= 0 &&
+         it.branch0 >= 0 && it.branch0 + last_row / p.G < p.nb &&
+         it.g >= 0 && it.g < p.Hkv && it.blk_begin >= 0 &&
+         it.blk_begin < it.blk_end && it.blk_end <= p.max_blocks &&
+         it.prow_base >= 0 &&
+         (int64_t)it.prow_base + it.nrows <= p.partial_rows;
+}
+
+template <int D, int NS>
+struct SplitCfg {
+  static constexpr int kWarps = 4;
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kTileBytes = 16 * D * 2;      // one (block, head) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;  // K + V
+  static constexpr int kRingBytes = kWarps * NS * kStageBytes;
+  static constexpr int kMergeBytes = kWarps * 16 * D * 4;
+  static constexpr int kSmem =
+      (kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes) + 1024;
+};
+
+template <int D, int NS>
+__global__ void __launch_bounds__(128, 1)
+    splitkv_decode_kernel(const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV,
+                          const SplitParams p) {
+  using C = SplitCfg<D, NS>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[C::kWarps][NS];
+  __shared__ float m_sh[C::kWarps][16];
+  __shared__ float l_sh[C::kWarps][16];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  float* base_ptr = reinterpret_cast<float*>(
+      smem_raw + (base - smem_u32(smem_raw)));
+  const WorkItem it = p.items[blockIdx.x];
+  if (!item_ok(it, p, 16)) {
+    if (threadIdx.x == 0) record_status(p.status, KV_ERR_DEVICE, -1 - (int)blockIdx.x);
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < C::kWarps; ++w)
+      for (int s = 0; s < NS; ++s) mbar_init(smem_u32(&bars[w][s]), 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  __syncthreads();
+
+  const int G = p.G;
+  const int seq_len = it.masked ? p.seq_lens[it.branch0] : 0x7fffffff;
+  const int32_t* table = p.tables + (int64_t)it.branch0 * p.max_blocks;
+  const int nblk = it.blk_end - it.blk_begin;
+  const int my_n = nblk > warp ? (nblk - warp + C::kWarps - 1) / C::kWarps : 0;
+  const uint32_t ring = base + warp * NS * C::kStageBytes;
+  const uint32_t bar0 = smem_u32(&bars[warp][0]);
+
+  // Issue the loads of this warp's k-th block into stage k % NS.  Returns
+  // whether the block id is inside the pool (uniform across the warp: every
+  // lane reads the same table entry).
+  auto issue = [&](int k) -> bool {
+    const int j = it.blk_begin + warp + C::kWarps * k;
+    const int phys = table[j];
+    const bool ok = phys >= 0 && (int64_t)phys < p.num_blocks;
+    const int s = k % NS;
+    const uint32_t st = ring + s * C::kStageBytes;
+    const uint32_t bar = bar0 + s * 8;
+    if (lane == 0) {
+      if (ok) {
+        fence_proxy_async_smem();
+        mbar_expect_tx(bar, C::kStageBytes);
+        const int y = (phys * p.Hkv + it.g) * 16;
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx) {
+          tma_load_2d(st + bx * 2048, &tmK, bx * 64, y, bar);
+          tma_load_2d(st + C::kTileBytes + bx * 2048, &tmV, bx * 64, y, bar);
+        }
+      } else {
+        record_status(p.status, KV_ERR_DEVICE, phys);
+        mbar_arrive(bar);
+      }
+    }
+    return ok;
+  };
+
+  uint32_t bad = 0;  // bit s: the block in stage s is outside the pool
+  const int pre = my_n < NS ? my_n : NS;
+  for (int k = 0; k < pre; ++k) {
+    if (!issue(k)) bad |= 1u << k;
+  }
+
+  // Query fragments (A operand, 16 rows x D): row r -> branch / q-head.
+  const int gq = lane >> 2, tq = lane & 3;
+  uint32_t qa[D / 16][4];
+  {
+    const __nv_bfloat16* rowp[2] = {nullptr, nullptr};
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int r = gq + 8 * hr;
+      if (r < it.nrows) {
+        const int rr = it.row0 + r;
+        const int b = it.branch0 + rr / G;
+        const int qh = it.g * G + rr % G;
+        rowp[hr] = p.q + ((int64_t)b * p.Hq + qh) * D;
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int hr = i & 1;
+        const int col = kk * 16 + 2 * tq + 8 * (i >> 1);
+        qa[kk][i] = rowp[hr]
+                        ? *reinterpret_cast<const uint32_t*>(rowp[hr] + col)
+                        : 0u;
+      }
+    }
+  }
+
+  float m_r[2] = {-INFINITY, -INFINITY};
+  float l_r[2] = {0.f, 0.f};
+  float o[D / 8][4];
+#pragma unroll
+  for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[nt][i] = 0.f;
+
+  const int mi = lane >> 3, ri = lane & 7;
+  bool timed_out = false;
+  int k = 0;
+  for (; k < my_n; ++k) {
+    const int s = k % NS;
+    const uint32_t st = ring + s * C::kStageBytes;
+    if (!mbar_wait(bar0 + s * 8, (k / NS) & 1)) {
+      timed_out = true;
+      break;
+    }
+    const int j = it.blk_begin + warp + C::kWarps * k;
+    if (!((bad >> s) & 1)) {
+      int nv = seq_len - j * 16;
+      nv = nv > 16 ? 16 : nv;
+      const uint32_t kt = st, vt = st + C::kTileBytes;
+      // S = Q K^T for the block's 16 tokens.
+      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int token = ((mi >> 1) << 3) + ri;
+        const int chunk = kk * 2 + (mi & 1);
+        const uint32_t addr = kt + (chunk >> 3) * 2048 + token * 128 +
+                              (((chunk & 7) ^ (token & 7)) << 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(addr, b0, b1, b2, b3);
+        mma_16816(sacc[0], qa[kk], b0, b1);
+        mma_16816(sacc[1], qa[kk], b2, b3);
+      }
+      // Scale, mask tokens past the branch's length, online softmax.
+      float x[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int tok = nt * 8 + 2 * tq + (i & 1);
+          x[nt][i] = tok < nv ? sacc[nt][i] * p.scale_log2 : -INFINITY;
+        }
+      float pr[2][4];
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        float mx = fmaxf(fmaxf(x[0][2 * hr], x[0][2 * hr + 1]),
+                         fmaxf(x[1][2 * hr], x[1][2 * hr + 1]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_r[hr], mx);
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = ex2(m_r[hr] - m_use);
+        m_r[hr] = m_new;
+        float sum = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float pv = ex2(x[nt][2 * hr + e] - m_use);
+            pr[nt][2 * hr + e] = pv;
+            sum += pv;
+          }
+        l_r[hr] = l_r[hr] * alpha + sum;
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) {
+          o[nt][2 * hr] *= alpha;
+          o[nt][2 * hr + 1] *= alpha;
+        }
+      }
+      // Masked slots may hold anything (even NaN): zero their V rows so that
+      // 0 * V stays 0 in the product below.
+      if (nv < 16) {
+        const int chunks = (16 - nv) * C::kBoxes * 8;
+        for (int c = lane; c < chunks; c += 32) {
+          const int row = nv + c / (C::kBoxes * 8);
+          const int rem = c % (C::kBoxes * 8);
+          st_shared_zero16(vt + (rem >> 3) * 2048 + row * 128 + (rem & 7) * 16);
+        }
+        // Order these generic-proxy writes before the TMA refill of the slot.
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      uint32_t pa[4];
+      pa[0] = pack_bf16(pr[0][0], pr[0][1]);
+      pa[1] = pack_bf16(pr[0][2], pr[0][3]);
+      pa[2] = pack_bf16(pr[1][0], pr[1][1]);
+      pa[3] = pack_bf16(pr[1][2], pr[1][3]);
+      // O += P V.
+#pragma unroll
+      for (int np = 0; np < D / 16; ++np) {
+        const int token = ((mi & 1) << 3) + ri;
+        const int chunk = np * 2 + (mi >> 1);
+        const uint32_t addr = vt + (chunk >> 3) * 2048 + token * 128 +
+                              (((chunk & 7) ^ (token & 7)) << 4);
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_t(addr, v0, v1, v2, v3);
+        mma_16816(o[2 * np], pa, v0, v1);
+        mma_16816(o[2 * np + 1], pa, v2, v3);
+      }
+    }
+    __syncwarp();
+    if (k + NS < my_n) {
+      if (issue(k + NS))
+        bad &= ~(1u << s);
+      else
+        bad |= 1u << s;
+    }
+  }
+  if (timed_out) {
+    if (lane == 0) record_status(p.status, KV_ERR_TIMEOUT, 1);
+    // Let every copy still in flight land before the CTA can exit.
+    for (int kk = k; kk < my_n && kk < k + NS; ++kk)
+      mbar_wait(bar0 + (kk % NS) * 8, (kk / NS) & 1);
+  }
+
+  // Row sums across the four lanes of each row.
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], 1);
+    l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], 2);
+  }
+
+  // Combine the four warps' partial states through shared memory.
+  __syncthreads();  // every warp is done with its ring
+  float* Ow = base_ptr + warp * 16 * D;
+#pragma unroll
+  for (int nt = 0; nt < D / 8; ++nt) {
+    const int col = nt * 8 + 2 * tq;
+    *reinterpret_cast<float2*>(Ow + gq * D + col) = make_float2(o[nt][0], o[nt][1]);
+    *reinterpret_cast<float2*>(Ow + (gq + 8) * D + col) =
+        make_float2(o[nt][2], o[nt][3]);
+  }
+  if (tq == 0) {
+    m_sh[warp][gq] = m_r[0];
+    m_sh[warp][gq + 8] = m_r[1];
+    l_sh[warp][gq] = l_r[0];
+    l_sh[warp][gq + 8] = l_r[1];
+  }
+  __syncthreads();
+  {
+    const int row = threadIdx.x >> 3;          // 16 rows x 8 threads
+    const int c0 = (threadIdx.x & 7) * (D / 8);
+    if (row < it.nrows) {
+      float mstar = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < C::kWarps; ++w) mstar = fmaxf(mstar, m_sh[w][row]);
+      const float muse = mstar == -INFINITY ? 0.f : mstar;
+      float wgt[C::kWarps];
+      float lstar = 0.f;
+#pragma unroll
+      for (int w = 0; w < C::kWarps; ++w) {
+        wgt[w] = ex2(m_sh[w][row] - muse);
+        lstar += wgt[w] * l_sh[w][row];
+      }
+      float* dst = p.o + (int64_t)(it.prow_base + row) * D + c0;
+#pragma unroll
+      for (int c = 0; c < D / 8; c += 4) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < C::kWarps; ++w) {
+          const float4 v = *reinterpret_cast<const float4*>(
+              base_ptr + (w * 16 + row) * D + c0 + c);
+          acc.x += wgt[w] * v.x;
+          acc.y += wgt[w] * v.y;
+          acc.z += wgt[w] * v.z;
+          acc.w += wgt[w] * v.w;
+        }
+        *reinterpret_cast<float4*>(dst + c) = acc;
+      }
+      if ((threadIdx.x & 7) == 0) p.ml[it.prow_base + row] = make_float2(mstar, lstar);
+    }
+  }
+}
+
+struct MergeParams {
+  const int32_t* csr_ptr;
+  const MergeEntry* csr;
+  const float2* ml;
+  const float* o;
+  __nv_bfloat16* out;
+  int nb, Hq, G;
+  int64_t partial_rows;
+};
+
+// One warp per (branch, q-head).
+template <int D>
+__global__ void __launch_bounds__(256) lse_merge_kernel(const MergeParams p) {
+  constexpr int V = D / 32;  // values per lane
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= p.nb * p.Hq) return;
+  const int b = gw / p.Hq, h = gw % p.Hq;
+  const int g = h / p.G, r = h % p.G;
+  const int e0 = p.csr_ptr[b], e1 = p.csr_ptr[b + 1];
+  float mstar = -INFINITY;
+  for (int e = e0; e < e1; ++e) {
+    const MergeEntry me = p.csr[e];
+    if (r < me.r_lo || r >= me.r_hi) continue;
+    const int64_t row = me.base + (int64_t)g * me.stride + (r - me.r_lo);
+    if (row < 0 || row >= p.partial_rows) continue;
+    mstar = fmaxf(mstar, p.ml[row].x);
+  }
+  const float muse = mstar == -INFINITY ? 0.f : mstar;
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  float lsum = 0.f;
+  for (int e = e0; e < e1; ++e) {
+    const MergeEntry me = p.csr[e];
+    if (r < me.r_lo || r >= me.r_hi) continue;
+    const int64_t row = me.base + (int64_t)g * me.stride + (r - me.r_lo);
+    if (row < 0 || row >= p.partial_rows) continue;
+    const float2 ml = p.ml[row];
+    const float w = ex2(ml.x - muse);
+    lsum += w * ml.y;
+    const float* src = p.o + (int64_t)row * D + lane * V;
+    if constexpr (V == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(src);
+      acc[0] += w * v.x; acc[1] += w * v.y;
+    }
+  }
+  const float inv = 1.f / lsum;
+  __nv_bfloat16* dst = p.out + ((int64_t)b * p.Hq + h) * D + lane * V;
+  if constexpr (V == 4) {
+    uint2 pk;
+    pk.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+    pk.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(dst) = pk;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
+  }
+}
+
+// ---- host side ----------------------------------------------------------------
+
+namespace {
+
+constexpr int kStages = 4;
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D view of one layer's pool: rows = block * Hkv * 16 + head * 16 + slot,
+// columns = head_dim; boxes of 16 rows x 64 columns, 128-byte swizzle.
+kv_status make_pool_map(CUtensorMap* tm, const void* pool, int64_t rows, int d) {
+  auto enc = get_encode();
+  if (!enc) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(pool), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return KV_OK;
+}
+
+template <int D>
+cudaError_t launch_split(const CUtensorMap& tk, const CUtensorMap& tv,
+                         const SplitParams& sp, int n_items,
+                         cudaStream_t stream) {
+  using C = SplitCfg<D, kStages>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(
+        splitkv_decode_kernel<D, kStages>,
+        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  splitkv_decode_kernel<D, kStages><<<n_items, 128, C::kSmem, stream>>>(tk, tv,
+                                                                        sp);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_merge(const MergeParams& mp, cudaStream_t stream) {
+  const int warps = mp.nb * mp.Hq;
+  lse_merge_kernel<D><<<(warps + 7) / 8, 256, 0, stream>>>(mp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Tensor-core (tcgen05) kernel for 128-row tiles; defined in decode_tc.cu.
+cudaError_t launch_tile_items(const CUtensorMap& tk, const CUtensorMap& tv,
+                              const SplitParams& sp, const WorkItem* items,
+                              int n_items, int d, cudaStream_t stream);
+
+thread_local void* const* g_launch_events = nullptr;
+thread_local int g_n_launch_events = 0;
+
+inline void mark(int slot, cudaStream_t st) {
+  if (slot < g_n_launch_events && g_launch_events[slot])
+    cudaEventRecord(static_cast<cudaEvent_t>(g_launch_events[slot]), st);
+}
+
+}  // namespace pkv
+
+using pkv::fail;
+
+extern "C" kv_status kv_set_launch_events(void* const* events,
+                                          int32_t n_events) {
+  pkv::clear_error();
+  pkv::g_launch_events = n_events > 0 ? events : nullptr;
+  pkv::g_n_launch_events = events ? n_events : 0;
+  return KV_OK;
+}
+
+extern "C" kv_status paged_decode_attn(
+    const void* q, const void* k_pool, const void* v_pool, int64_t num_blocks,
+    const int32_t* block_tables, const int32_t* seq_lens,
+    const int32_t* prefix_groups, int32_t n_groups, int32_t nb,
+    int32_t max_blocks, int32_t Hq, int32_t Hkv, int32_t d, int32_t block_size,
+    float scale, void* out, const int32_t* plan,
+    const kv_decode_plan_info* info, void* workspace, size_t ws_bytes,
+    void* stream) {
+  pkv::clear_error();
+  (void)prefix_groups;
+  if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out ||
+      !plan || !info || !workspace)
+    return fail(KV_ERR_INVALID_ARG, "null argument");
+  if (n_groups < 0 || (n_groups > 0 && !prefix_groups))
+    return fail(KV_ERR_INVALID_ARG, "bad prefix_groups");
+  if (nb < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_blocks < 1)
+    return fail(KV_ERR_INVALID_ARG, "bad nb/Hq/Hkv/max_blocks");
+  if (d != 64 && d != 128) return fail(KV_ERR_INVALID_ARG, "head_dim 64 or 128");
+  if (block_size != 16) return fail(KV_ERR_INVALID_ARG, "block_size must be 16");
+  if (num_blocks < 1 || num_blocks * Hkv * 16 > (int64_t)INT32_MAX)
+    return fail(KV_ERR_INVALID_ARG, "num_blocks out of range");
+  if (((uintptr_t)q | (uintptr_t)k_pool | (uintptr_t)v_pool | (uintptr_t)out) & 15)
+    return fail(KV_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned");
+  if ((uintptr_t)workspace & 255)
+    return fail(KV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (!std::isfinite(scale)) return fail(KV_ERR_INVALID_ARG, "scale not finite");
+  if (info->n_merge_rows != nb || info->partial_rows < 0)
+    return fail(KV_ERR_INVALID_ARG, "plan info does not match nb");
+  const size_t need = pkv::ws_total(info->partial_rows, d);
+  if (ws_bytes < need || (size_t)info->workspace_bytes != need)
+    return fail(KV_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed",
+                ws_bytes, need);
+
+  cudaStream_t st = (cudaStream_t)stream;
+  CUtensorMap tk, tv;
+  const int64_t rows = num_blocks * Hkv * 16;
+  if (kv_status s = pkv::make_pool_map(&tk, k_pool, rows, d)) return s;
+  if (kv_status s = pkv::make_pool_map(&tv, v_pool, rows, d)) return s;
+
+  auto* ws = static_cast<uint8_t*>(workspace);
+  pkv::SplitParams sp;
+  sp.q = static_cast<const __nv_bfloat16*>(q);
+  sp.tables = block_tables;
+  sp.seq_lens = seq_lens;
+  sp.ml = reinterpret_cast<float2*>(ws + pkv::ws_ml_offset());
+  sp.o = reinterpret_cast<float*>(ws + pkv::ws_o_offset(info->partial_rows));
+  sp.status = reinterpret_cast<pkv::DeviceStatus*>(ws);
+  sp.nb = nb;
+  sp.partial_rows = info->partial_rows;
+  sp.Hq = Hq;
+  sp.Hkv = Hkv;
+  sp.G = Hq / Hkv;
+  sp.max_blocks = max_blocks;
+  sp.num_blocks = num_blocks;
+  sp.scale_log2 = scale * 1.4426950408889634f;
+
+  // The plan lives on the device; its layout is fixed by the host header
+  // fields mirrored in *info.
+  const int off_row = pkv::kPlanHeaderInts;
+  const int off_tile = off_row + 8 * info->n_row_items;
+  const int off_ptr = off_tile + 8 * info->n_tile_items;
+  const int off_ent = off_ptr + nb + 1;
+
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(pkv::DeviceStatus), st);
+  if (e != cudaSuccess) return fail(KV_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+  if (info->n_tile_items > 0) {
+    pkv::mark(0, st);
+    e = pkv::launch_tile_items(
+        tk, tv, sp, reinterpret_cast<const pkv::WorkItem*>(plan + off_tile),
+        info->n_tile_items, d, st);
+    pkv::mark(1, st);
+    if (e != cudaSuccess)
+      return fail(KV_ERR_CUDA, "tile kernel: %s", cudaGetErrorString(e));
+  }
+  if (info->n_row_items > 0) {
+    sp.items = reinterpret_cast<const pkv::WorkItem*>(plan + off_row);
+    pkv::mark(2, st);
+    e = d == 128 ? pkv::launch_split<128>(tk, tv, sp, info->n_row_items, st)
+                 : pkv::launch_split<64>(tk, tv, sp, info->n_row_items, st);
+    pkv::mark(3, st);
+    if (e != cudaSuccess)
+      return fail(KV_ERR_CUDA, "split-KV kernel: %s", cudaGetErrorString(e));
+  }
+  pkv::MergeParams mp;
+  mp.csr_ptr = plan + off_ptr;
+  mp.csr = reinterpret_cast<const pkv::MergeEntry*>(plan + off_ent);
+  mp.ml = sp.ml;
+  mp.o = sp.o;
+  mp.out = static_cast<__nv_bfloat16*>(out);
+  mp.nb = nb;
+  mp.Hq = Hq;
+  mp.G = sp.G;
+  mp.partial_rows = info->partial_rows;
+  pkv::mark(4, st);
+  e = d == 128 ? pkv::launch_merge<128>(mp, st) : pkv::launch_merge<64>(mp, st);
+  pkv::mark(5, st);
+  if (e != cudaSuccess)
+    return fail(KV_ERR_CUDA, "merge kernel: %s", cudaGetErrorString(e));
+  return KV_OK;
+}
+
+extern "C" kv_status kv_check_device_status(void* workspace, void* stream,
+                                            int32_t* out_code,
+                                            int32_t* out_detail) {
+  pkv::clear_error();
+  if (!workspace || !out_code) return fail(KV_ERR_INVALID_ARG, "null argument");
+  pkv::DeviceStatus h{};
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(&h, workspace, sizeof h,
+                                  cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof h, st);
+  if (e != cudaSuccess)
+    return fail(KV_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  *out_code = (int32_t)h.code;
+  if (out_detail) *out_detail = h.detail;
+  return KV_OK;
+}

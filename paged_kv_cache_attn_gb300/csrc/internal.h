@@ -1,0 +1,84 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <cstdio>
+#include <string>
+#include <vector>
+
+#include "pagedkv.h"
+
+namespace pkv {
+
+// ---- errors ---------------------------------------------------------------
+kv_status fail(kv_status code, const char* fmt, ...);
+void clear_error();
+
+// ---- plan format ----------------------------------------------------------
+// A plan is an int32 array: a header, the split-KV work items, the tensor-core
+// work items, and a CSR list telling the merge pass which partial rows belong
+// to each branch.
+constexpr int32_t kPlanMagic = 0x31564B50;  // "PKV1"
+constexpr int kPlanHeaderInts = 16;
+enum PlanHeader {
+  H_MAGIC = 0, H_NB, H_HQ, H_HKV, H_D, H_N_ROW_ITEMS, H_N_TILE_ITEMS, H_N_CSR,
+  H_OFF_ROW_ITEMS, H_OFF_TILE_ITEMS, H_OFF_CSR_PTR, H_OFF_CSR_ENT,
+  H_PARTIAL_ROWS, H_CHUNK, H_FLAGS, H_TOTAL
+};
+
+// One work item: query rows [row0, row0 + nrows) of a unit whose first branch
+// is `branch0` (row r -> branch branch0 + r / G, q-head g * G + r % G), over
+// logical blocks [blk_begin, blk_end) of branch0's table, for kv-head g.
+// Partial results go to rows prow_base .. prow_base + nrows - 1.
+// masked != 0: the unit is a single branch whose last block may be partial;
+// tokens at or past seq_lens[branch0] are excluded.
+struct WorkItem {
+  int32_t branch0, g, row0, nrows, blk_begin, blk_end, prow_base, masked;
+};
+static_assert(sizeof(WorkItem) == 32, "WorkItem is 8 int32");
+
+// Merge entry for one branch: q-heads-in-group [r_lo, r_hi) of this branch
+// have partial rows base + g * stride + (r - r_lo) for kv-head g.
+struct MergeEntry {
+  int32_t base, stride, r_lo, r_hi;
+};
+
+constexpr bool kTensorCoreKernel = false;  // tcgen05 tile kernel available
+constexpr int kTileRows = 128;      // rows of a tcgen05 tile
+constexpr int kRowTile = 16;        // rows of an mma.sync tile
+constexpr int kMinTensorRows = 65;  // segments with more rows go to tcgen05
+
+// Workspace layout (bytes): status word block, then (m, l) pairs, then o rows.
+constexpr size_t kStatusBytes = 256;
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline size_t ws_ml_offset() { return kStatusBytes; }
+inline size_t ws_o_offset(int64_t rows) {
+  return align_up(kStatusBytes + (size_t)rows * 8, 256);
+}
+inline size_t ws_total(int64_t rows, int d) {
+  return align_up(ws_o_offset(rows) + (size_t)rows * d * 4, 256);
+}
+
+// Device status word (first 16 bytes of the workspace).
+struct DeviceStatus {
+  uint32_t code;    // 0, KV_ERR_DEVICE or KV_ERR_TIMEOUT (first recorded)
+  int32_t detail;   // first bad value (block id, item index, wait site)
+  uint32_t count;   // how many events were recorded
+  uint32_t pad;
+};
+
+// ---- kernel launchers (state_kernels.cu, decode kernels) -------------------
+// Copy appended K/V rows into their slots.  dst_blocks[i] = physical block of
+// logical block first_lblock + i; rows are tokens [tok0, tok0 + n) of the
+// branch (tok0 = its seq_len before the append).
+int launch_append_scatter(void* k_pool, void* v_pool, const void* k_new,
+                          const void* v_new, int64_t num_blocks, int L,
+                          int Hkv, int d, int B, int n, int tok0,
+                          const int32_t* dst_blocks, int n_dst,
+                          void* stream);
+// Copy whole blocks src[i] -> dst[i] (every layer, K and V).
+int launch_block_copy(void* k_pool, void* v_pool, int64_t num_blocks, int L,
+                      int Hkv, int d, int B, const int32_t* src,
+                      const int32_t* dst, int n, void* stream);
+
+}  // namespace pkv

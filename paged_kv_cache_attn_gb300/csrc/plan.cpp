@@ -1,0 +1,227 @@
+// Host half of a decode step: cut the step into work items for the split-KV
+// kernel (rows <= 16 per item), the tcgen05 kernel (128-row tiles of large
+// shared-prefix segments) and the LSE merge.
+//
+// Each branch's logical blocks are covered exactly once: by the segments that
+// contain its row (which tile [0, shared_end) -- each segment's blocks are
+// read once for all of its rows) and by its own suffix [shared_end, n_blocks).
+// Every item writes unnormalised partial results (o, m, l) per query row; the
+// merge combines a row's partials by their log-sum-exp.  The split sizes do
+// not change the result beyond rounding.
+
+#include <algorithm>
+#include <cstring>
+#include <numeric>
+
+#include "internal.h"
+
+using pkv::fail;
+
+namespace {
+
+struct Unit {
+  int32_t branch0, rows, blk_begin, blk_end, masked;
+  bool tile;  // tcgen05 128-row tiles
+};
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int32_t pick_chunk(const std::vector<Unit>& units, bool tile, int Hkv,
+                   int num_sms, int32_t start) {
+  const int rows_per = tile ? pkv::kTileRows : pkv::kRowTile;
+  int32_t chunk = start;
+  for (;;) {
+    int64_t items = 0;
+    for (const Unit& u : units) {
+      if (u.tile != tile) continue;
+      items += ceil_div(u.blk_end - u.blk_begin, chunk) *
+               ceil_div(u.rows, rows_per) * Hkv;
+    }
+    if (chunk <= 8 || items >= 2LL * num_sms) return chunk;
+    chunk /= 2;
+  }
+}
+
+}  // namespace
+
+extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
+                                       int32_t d, int32_t B,
+                                       int32_t max_blocks,
+                                       const int32_t* seq_lens,
+                                       const int32_t* groups, int32_t n_groups,
+                                       int32_t num_sms, int32_t flags,
+                                       int32_t* plan, int64_t plan_cap,
+                                       kv_decode_plan_info* info) {
+  pkv::clear_error();
+  if (!info || !seq_lens) return fail(KV_ERR_INVALID_ARG, "null argument");
+  if (nb < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+    return fail(KV_ERR_INVALID_ARG, "bad nb/Hq/Hkv (%d/%d/%d)", nb, Hq, Hkv);
+  if (d != 64 && d != 128)
+    return fail(KV_ERR_INVALID_ARG, "head_dim must be 64 or 128");
+  if (B != 16) return fail(KV_ERR_INVALID_ARG, "block_size must be 16");
+  if (max_blocks < 1) return fail(KV_ERR_INVALID_ARG, "max_blocks must be >= 1");
+  if (n_groups < 0 || (n_groups > 0 && !groups))
+    return fail(KV_ERR_INVALID_ARG, "bad groups");
+  if (num_sms <= 0) num_sms = 152;
+  const int32_t G = Hq / Hkv;
+
+  std::vector<int32_t> nblk(nb);
+  for (int32_t b = 0; b < nb; ++b) {
+    if (seq_lens[b] < 1 || (int64_t)seq_lens[b] > (int64_t)max_blocks * B)
+      return fail(KV_ERR_INVALID_ARG, "seq_lens[%d] = %d outside [1, %lld]", b,
+                  seq_lens[b], (long long)max_blocks * B);
+    nblk[b] = (seq_lens[b] + B - 1) / B;
+  }
+
+  // Segments: validate and find each row's shared end.
+  std::vector<int32_t> shared_end(nb, 0);
+  std::vector<Unit> units;
+  const bool use_groups = !(flags & KV_PLAN_IGNORE_GROUPS);
+  const bool allow_tc =
+      pkv::kTensorCoreKernel && !(flags & KV_PLAN_NO_TENSOR_CORES);
+  if (use_groups && n_groups > 0) {
+    std::vector<std::vector<std::pair<int32_t, int32_t>>> per_row(nb);
+    for (int32_t i = 0; i < n_groups; ++i) {
+      const int32_t* s = groups + 4 * (int64_t)i;
+      const int32_t bb = s[0], bc = s[1], kb = s[2], kc = s[3];
+      if (bb < 0 || bc < 1 || (int64_t)bb + bc > nb || kb < 0 || kc < 1)
+        return fail(KV_ERR_INVALID_ARG, "segment %d {%d,%d,%d,%d} malformed",
+                    i, bb, bc, kb, kc);
+      if ((int64_t)bc * G > INT32_MAX / 2)
+        return fail(KV_ERR_INVALID_ARG, "segment %d too many rows", i);
+      for (int32_t b = bb; b < bb + bc; ++b) {
+        if ((int64_t)(kb + kc) * B > seq_lens[b])
+          return fail(KV_ERR_INVALID_ARG,
+                      "segment %d covers a block not full for row %d", i, b);
+        per_row[b].push_back({kb, kb + kc});
+      }
+      units.push_back({bb, bc * G, kb, kb + kc, 0,
+                       allow_tc && bc * G >= pkv::kMinTensorRows});
+    }
+    for (int32_t b = 0; b < nb; ++b) {
+      auto& v = per_row[b];
+      std::sort(v.begin(), v.end());
+      int32_t end = 0;
+      for (auto& [lo, hi] : v) {
+        if (lo != end)
+          return fail(KV_ERR_INVALID_ARG,
+                      "row %d: segments do not tile [0, end) (gap or overlap "
+                      "at block %d)", b, lo);
+        end = hi;
+      }
+      shared_end[b] = end;
+    }
+  }
+  for (int32_t b = 0; b < nb; ++b) {
+    if (shared_end[b] < nblk[b])
+      units.push_back({b, G, shared_end[b], nblk[b], 1, false});
+  }
+
+  const int32_t chunk_rows = pick_chunk(units, false, Hkv, num_sms, 64);
+  const int32_t chunk_tile = pick_chunk(units, true, Hkv, num_sms, 128);
+
+  std::vector<pkv::WorkItem> row_items, tile_items;
+  std::vector<std::vector<pkv::MergeEntry>> merge(nb);
+  int64_t prow = 0;
+  for (const Unit& u : units) {
+    const int rows_per = u.tile ? pkv::kTileRows : pkv::kRowTile;
+    const int32_t chunk = u.tile ? chunk_tile : chunk_rows;
+    const int32_t len = u.blk_end - u.blk_begin;
+    const int32_t nch = (int32_t)ceil_div(len, chunk);
+    for (int32_t c = 0; c < nch; ++c) {
+      // Even split of the range into nch pieces.
+      const int32_t lo = u.blk_begin + (int32_t)((int64_t)len * c / nch);
+      const int32_t hi = u.blk_begin + (int32_t)((int64_t)len * (c + 1) / nch);
+      for (int32_t row0 = 0; row0 < u.rows; row0 += rows_per) {
+        const int32_t nrows = std::min(rows_per, u.rows - row0);
+        const int64_t base0 = prow;
+        for (int32_t g = 0; g < Hkv; ++g) {
+          pkv::WorkItem it{u.branch0, g, row0, nrows, lo, hi,
+                           (int32_t)(base0 + (int64_t)g * nrows), u.masked};
+          (u.tile ? tile_items : row_items).push_back(it);
+        }
+        prow += (int64_t)nrows * Hkv;
+        if (prow > INT32_MAX)
+          return fail(KV_ERR_INVALID_ARG, "step too large for one plan");
+        // Merge entries for every branch these rows touch.
+        const int32_t row1 = row0 + nrows;
+        for (int32_t pb = row0 / G; pb * G < row1; ++pb) {
+          const int32_t a = std::max(row0, pb * G);
+          const int32_t e = std::min(row1, pb * G + G);
+          merge[u.branch0 + pb].push_back(
+              {(int32_t)(base0 + (a - row0)), nrows, a - pb * G, e - pb * G});
+        }
+      }
+    }
+  }
+  // Longest items first: the last wave is made of the short ones.
+  auto by_len = [](const pkv::WorkItem& x, const pkv::WorkItem& y) {
+    return (x.blk_end - x.blk_begin) > (y.blk_end - y.blk_begin);
+  };
+  std::stable_sort(row_items.begin(), row_items.end(), by_len);
+  std::stable_sort(tile_items.begin(), tile_items.end(), by_len);
+
+  int64_t n_csr = 0;
+  for (auto& m : merge) n_csr += (int64_t)m.size();
+  const int64_t off_row = pkv::kPlanHeaderInts;
+  const int64_t off_tile = off_row + 8 * (int64_t)row_items.size();
+  const int64_t off_ptr = off_tile + 8 * (int64_t)tile_items.size();
+  const int64_t off_ent = off_ptr + nb + 1;
+  const int64_t total = off_ent + 4 * n_csr;
+  if (total > INT32_MAX) return fail(KV_ERR_INVALID_ARG, "plan too large");
+
+  info->plan_ints = total;
+  info->partial_rows = prow;
+  info->workspace_bytes = (int64_t)pkv::ws_total(prow, d);
+  info->n_row_items = (int32_t)row_items.size();
+  info->n_tile_items = (int32_t)tile_items.size();
+  info->n_merge_rows = nb;
+  info->chunk_blocks = chunk_rows;
+  if (!plan) return KV_OK;
+  if (plan_cap < total)
+    return fail(KV_ERR_INVALID_ARG, "plan_cap %lld < %lld", (long long)plan_cap,
+                (long long)total);
+  int32_t* h = plan;
+  std::fill(h, h + pkv::kPlanHeaderInts, 0);
+  h[pkv::H_MAGIC] = pkv::kPlanMagic;
+  h[pkv::H_NB] = nb;
+  h[pkv::H_HQ] = Hq;
+  h[pkv::H_HKV] = Hkv;
+  h[pkv::H_D] = d;
+  h[pkv::H_N_ROW_ITEMS] = (int32_t)row_items.size();
+  h[pkv::H_N_TILE_ITEMS] = (int32_t)tile_items.size();
+  h[pkv::H_N_CSR] = (int32_t)n_csr;
+  h[pkv::H_OFF_ROW_ITEMS] = (int32_t)off_row;
+  h[pkv::H_OFF_TILE_ITEMS] = (int32_t)off_tile;
+  h[pkv::H_OFF_CSR_PTR] = (int32_t)off_ptr;
+  h[pkv::H_OFF_CSR_ENT] = (int32_t)off_ent;
+  h[pkv::H_PARTIAL_ROWS] = (int32_t)prow;
+  h[pkv::H_CHUNK] = chunk_rows;
+  h[pkv::H_FLAGS] = flags;
+  h[pkv::H_TOTAL] = (int32_t)total;
+  std::memcpy(h + off_row, row_items.data(), row_items.size() * 32);
+  std::memcpy(h + off_tile, tile_items.data(), tile_items.size() * 32);
+  int32_t* ptr = h + off_ptr;
+  int32_t* ent = h + off_ent;
+  int64_t k = 0;
+  for (int32_t b = 0; b < nb; ++b) {
+    ptr[b] = (int32_t)k;
+    for (auto& e : merge[b]) {
+      ent[4 * k + 0] = e.base;
+      ent[4 * k + 1] = e.stride;
+      ent[4 * k + 2] = e.r_lo;
+      ent[4 * k + 3] = e.r_hi;
+      ++k;
+    }
+  }
+  ptr[nb] = (int32_t)k;
+  return KV_OK;
+}
+
+extern "C" kv_status paged_decode_attn_workspace_size(
+    const kv_decode_plan_info* info, size_t* out_bytes) {
+  pkv::clear_error();
+  if (!info || !out_bytes) return fail(KV_ERR_INVALID_ARG, "null argument");
+  *out_bytes = (size_t)info->workspace_bytes;
+  return KV_OK;
+}

@@ -1,0 +1,176 @@
+"""CUDA path vs the fp64 oracle, through the C ABI.
+
+Tolerance (the bound stated for this path: bf16 inputs, fp32 accumulation):
+element-wise |gpu - oracle| <= 2e-3 + 1e-2 * |oracle|.
+Allocator state and pool bytes: bit-exact.
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+from oracle import attention as att  # noqa: E402
+from oracle import replay as rp  # noqa: E402
+from paged_kv_cache_attn_gb300 import binding as B  # noqa: E402
+from paged_kv_cache_attn_gb300 import harness as H  # noqa: E402
+from paged_kv_cache_attn_gb300 import workloads as W  # noqa: E402
+
+ATOL, RTOL = 2e-3, 1e-2
+
+
+def bf16_bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def run_decode(cache, q_bits, flags=0):
+    bt = cache.batch(flags=flags).upload()
+    q = torch.from_numpy(q_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    out = torch.empty_like(q)
+    bt.decode(q, out)
+    torch.cuda.synchronize()
+    code, detail = bt.device_status()
+    assert code == 0, (code, detail)
+    return att.bf16_to_f64(bf16_bits(out)), bt
+
+
+def assert_close(gpu, ref, what=""):
+    err = np.abs(gpu - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside "
+                           f"tolerance; max abs err {err.max():.3g}")
+
+
+SMALL = {
+    "tiny_tree": lambda: W.tiny_tree(),
+    "tiny_tree_peaked": lambda: W.tiny_tree(q_gain=4.0),
+    "independent": lambda: W.independent(n_seqs=6, min_len=1, max_len=700),
+    "fanout": lambda: W.fanout(n_roots=2, root_tokens=256, fan=8,
+                               min_suffix=1, max_suffix=100),
+    "deep_tree": lambda: W.deep_tree(root_tokens=300, depth=3, min_seg=5,
+                                     max_seg=40),
+    "long_context": lambda: W.long_context(n_indep=3, indep_tokens=1000,
+                                           n_roots=2, root_tokens=2048,
+                                           fan=16, suffix_tokens=37),
+    "gqa_2": lambda: W.independent(n_seqs=3, min_len=17, max_len=300, Hq=8,
+                                   Hkv=4, d=64),
+    "gqa_16": lambda: W.fanout(n_roots=1, root_tokens=64, fan=3,
+                               min_suffix=1, max_suffix=30, Hq=32, Hkv=2),
+}
+
+
+@pytest.fixture(scope="module")
+def built():
+    assert torch.cuda.is_available()
+    return True
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("flags", [0, B.KV_PLAN_IGNORE_GROUPS,
+                                   B.KV_PLAN_NO_TENSOR_CORES])
+def test_decode_matches_oracle(built, name, flags):
+    w = SMALL[name]()
+    cache = H.Cache(w)
+    ref = rp.replay(w, with_data=True)
+    assert cache.decode_ids == ref.decode_ids
+    q = w.queries(len(cache.decode_ids))
+    gpu, _ = run_decode(cache, q, flags)
+    want = rp.decode_all_from_pool(ref, q, w.scale)
+    assert_close(gpu, want, name)
+
+
+@pytest.mark.parametrize("name", ["tiny_tree", "deep_tree", "fanout"])
+def test_pool_bytes_bit_exact(built, name):
+    """Appends and copy-on-write copies put every valid token's K/V rows in
+    the slot the oracle's own replay puts them."""
+    w = SMALL[name]()
+    cache = H.Cache(w)
+    ref = rp.replay(w, with_data=True)
+    torch.cuda.synchronize()
+    k = bf16_bits(cache.k)
+    v = bf16_bits(cache.v)
+    assert cache.tables() == {i: (n.table, n.seq_len)
+                              for i, n in enumerate(ref.model.nodes) if n.live}
+    for i, n in enumerate(ref.model.nodes):
+        if not n.live:
+            continue
+        t = np.arange(n.seq_len)
+        blk = np.asarray(n.table)[t // 16]
+        slot = t % 16
+        assert np.array_equal(k[:, blk, :, slot], ref.data.k[:, blk, :, slot])
+        assert np.array_equal(v[:, blk, :, slot], ref.data.v[:, blk, :, slot])
+
+
+def test_poisoned_free_slots_do_not_leak(built):
+    """Slots past a branch's length hold NaN: the output must not see them."""
+    w = SMALL["long_context"]()
+    cache = H.Cache.__new__(H.Cache)
+    # Build with NaN-filled pools: allocate, poison, then replay.
+    cache.w, cache.with_data, cache.device = w, True, "cuda"
+    shape = (w.num_layers, w.num_blocks, w.Hkv, w.block_size, w.d)
+    cache.k = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    cache.v = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    cache.h = B.kv_pool_create(w.num_blocks, w.num_layers, w.Hkv, w.d, cache.k,
+                               cache.v, w.initial_free_order())
+    cache.evicted = []
+    cache._replay()
+    cache.decode_ids = w.leaves()
+    ref = rp.replay(w, with_data=True)
+    q = w.queries(len(cache.decode_ids))
+    gpu, _ = run_decode(cache, q)
+    assert np.isfinite(gpu).all()
+    assert_close(gpu, rp.decode_all_from_pool(ref, q, w.scale), "poisoned")
+
+
+def test_physical_layout_does_not_change_the_output(built):
+    w1 = SMALL["fanout"]()
+    w2 = SMALL["fanout"]()
+    w2.initial_free_order = lambda: np.arange(w2.num_blocks, dtype=np.int32)
+    q = w1.queries(len(w1.leaves()))
+    a, _ = run_decode(H.Cache(w1), q)
+    b, _ = run_decode(H.Cache(w2), q)
+    assert np.array_equal(a, b)
+
+
+def test_bad_block_id_is_reported(built):
+    w = SMALL["independent"]()
+    cache = H.Cache(w)
+    bt = cache.batch().upload()
+    bt.dev["tables"][1, 2] = w.num_blocks + 5
+    q = torch.zeros((bt.nb, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    bt.decode(q, out)
+    code, detail = bt.device_status()
+    assert code == B.KV_ERR_DEVICE and detail == w.num_blocks + 5
+    # The status word is cleared by the read; a clean step reports 0.
+    bt.dev["tables"][1, 2] = int(bt.tables[1, 2])
+    bt.decode(q, out)
+    assert bt.device_status() == (0, 0)
+
+
+# ---- full sizes: sampled rows against the oracle ---------------------------
+
+FULL = ["independent", "fanout", "deep_tree", "long_context"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_rows(built, name):
+    w = W.CONFIGS[name]()
+    cache = H.Cache(w)
+    ref = rp.replay(w, with_data=False)
+    assert cache.decode_ids == ref.decode_ids
+    nb = len(cache.decode_ids)
+    q = w.queries(nb)
+    gpu, bt = run_decode(cache, q)
+    rng = np.random.default_rng(5)
+    rows = sorted(set([0, nb - 1] + rng.choice(nb, 4, replace=False).tolist()))
+    want = rp.decode_rows(ref, q, rows, w.scale)
+    for b in rows:
+        assert_close(gpu[b], want[b], f"{name} row {b}")
+    # Every output is finite and a convex combination of V rows: bounded by
+    # the largest |V| of a bf16 N(0,1) draw.
+    assert np.isfinite(gpu).all() and np.abs(gpu).max() < 8
+    cache.close()

@@ -1,0 +1,313 @@
+"""The library's host logic (allocator, tree, eviction, batch builder, plan)
+against the oracle's allocator model, bit-exact, on metadata-only pools (no
+GPU, no kernels)."""
+
+import json
+import os
+import random
+
+import numpy as np
+import pytest
+
+from oracle import allocator as al
+from oracle import attention as att
+from oracle import replay as rp
+from paged_kv_cache_attn_gb300 import binding as B
+from paged_kv_cache_attn_gb300 import harness as H
+from paged_kv_cache_attn_gb300 import workloads as W
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                     "pages_worked_examples.json")))
+
+SMALL = {
+    "tiny_tree": lambda: W.tiny_tree(),
+    "independent": lambda: W.independent(),
+    "fanout": lambda: W.fanout(),
+    "deep_tree": lambda: W.deep_tree(),
+    "long_context": lambda: W.long_context(),
+}
+
+
+def model_tables(m):
+    return {i: (n.table, n.seq_len) for i, n in enumerate(m.nodes) if n.live}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_workload_state_matches_oracle_bit_exact(name):
+    w = SMALL[name]()
+    lib = H.Cache(w, with_data=False)
+    ref = rp.replay(w, with_data=False)
+    assert lib.tables() == model_tables(ref.model)
+    assert lib.refcounts() == ref.model.ref
+    assert lib.free_stack() == ref.model.free_stack()
+    assert lib.evicted == ref.evicted
+    assert lib.decode_ids == ref.decode_ids
+
+
+def test_page_table_diagram_through_the_library():
+    g = GOLDEN["page_table_diagram"]
+    f = g["frames"]
+    order = [f["root_block_0"], f["branch_a_block_1"], f["branch_b_block_2"]]
+    order += [b for b in range(128) if b not in order]
+    h = B.kv_pool_create(128, 1, 1, 128, None, None, order)
+    root = B.kv_branch_create(h)
+    B.kv_append(h, root, 16)
+    a = B.kv_fork_branch(h, root)
+    b = B.kv_fork_branch(h, root)
+    B.kv_append(h, a, 16)
+    B.kv_append(h, b, 16)
+    assert B.kv_get_refcounts(h, 128)[f["root_block_0"]] == 3
+    B.kv_free(h, root)
+    ref = B.kv_get_refcounts(h, 128)
+    for blk, n in g["ref_counts"].items():
+        assert ref[int(blk)] == n
+    assert B.kv_get_block_table(h, a)[0].tolist() == [42, 87]
+    assert B.kv_get_block_table(h, b)[0].tolist() == [42, 103]
+    B.kv_pool_destroy(h)
+
+
+def _apply(lib_h, m, op):
+    """Run one op on both sides; return (lib outcome, model outcome)."""
+    kind = op[0]
+
+    def lib_call():
+        if kind == "create":
+            return B.kv_branch_create(lib_h)
+        if kind == "append":
+            return B.kv_append(lib_h, op[1], op[2])
+        if kind == "fork":
+            return B.kv_fork_branches(lib_h, op[1], op[2])
+        if kind == "free":
+            return B.kv_free(lib_h, op[1])
+        if kind == "subtree":
+            return B.kv_free_subtree(lib_h, op[1])
+        if kind == "evict":
+            return B.kv_evict(lib_h, op[1], op[2], op[3], op[4])
+        raise ValueError(kind)
+
+    def model_call():
+        if kind == "create":
+            return m.create()
+        if kind == "append":
+            m.append(op[1], op[2])
+            return None
+        if kind == "fork":
+            return [c for c, _ in m.fork_many(op[1], op[2])]
+        if kind == "free":
+            m.free_node(op[1])
+            return None
+        if kind == "subtree":
+            return m.free_subtree(op[1])
+        if kind == "evict":
+            return m.evict(op[1], op[2], op[3], op[4])
+        raise ValueError(kind)
+
+    def outcome(fn):
+        try:
+            return ("ok", fn())
+        except al.OutOfBlocks:
+            return ("oom", None)
+        except KeyError:
+            return ("notfound", None)
+        except B.KVError as e:
+            return ({B.KV_ERR_OOM: "oom", B.KV_ERR_NOT_FOUND: "notfound"}
+                    .get(e.code, f"err{e.code}"), None)
+
+    return outcome(lib_call), outcome(model_call)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_ops_match_oracle(seed):
+    rnd = random.Random(seed)
+    nblocks = rnd.choice([8, 40, 300])
+    order = list(range(nblocks))
+    rnd.shuffle(order)
+    h = B.kv_pool_create(nblocks, 2, 2, 64, None, None, order)
+    m = al.PoolModel(nblocks, 16, order)
+    ids = []
+    for step in range(250):
+        r = rnd.random()
+        if not ids or r < 0.08:
+            op = ("create",)
+        elif r < 0.45:
+            op = ("append", rnd.choice(ids + [len(ids) + 3]), rnd.randint(0, 50))
+        elif r < 0.7:
+            op = ("fork", rnd.choice(ids), rnd.randint(1, 4))
+        elif r < 0.82:
+            op = ("free", rnd.choice(ids))
+        elif r < 0.9:
+            op = ("subtree", rnd.choice(ids))
+        else:
+            cand = rnd.sample(ids, min(len(ids), 5))
+            scores = [rnd.random() for _ in cand]
+            op = ("evict", cand, scores, rnd.choice([0, 1]), rnd.randint(0, 6))
+        got, want = _apply(h, m, op)
+        assert got == want, (step, op)
+        if op[0] == "create" and got[0] == "ok":
+            ids.append(got[1])
+        if op[0] == "fork" and got[0] == "ok":
+            ids += got[1]
+        # Full state after every op.
+        assert B.kv_get_refcounts(h, nblocks).tolist() == m.ref
+        assert B.kv_get_free_stack(h).tolist() == m.free_stack()
+        for i in ids:
+            info = B.kv_branch_info(h, i)
+            nd = m.nodes[i]
+            assert info["live"] == int(nd.live)
+            assert info["depth"] == nd.depth and info["parent"] == nd.parent
+            if nd.live:
+                t, L = B.kv_get_block_table(h, i)
+                assert t.tolist() == nd.table and L == nd.seq_len
+        m.check_invariants()
+    B.kv_pool_destroy(h)
+
+
+def test_error_codes_and_atomicity():
+    h = B.kv_pool_create(4, 1, 1, 64)
+    r = B.kv_branch_create(h)
+    B.kv_append(h, r, 40)
+    before = (B.kv_get_refcounts(h, 4).tolist(), B.kv_get_free_stack(h).tolist())
+    with pytest.raises(B.KVError) as e:
+        B.kv_append(h, r, 40)
+    assert e.value.code == B.KV_ERR_OOM
+    with pytest.raises(B.KVError) as e:
+        B.kv_fork_branches(h, r, 2)
+    assert e.value.code == B.KV_ERR_OOM
+    assert (B.kv_get_refcounts(h, 4).tolist(),
+            B.kv_get_free_stack(h).tolist()) == before
+    assert B.kv_num_branches(h) == 1
+    with pytest.raises(B.KVError) as e:
+        B.kv_fork_branch(h, 9)
+    assert e.value.code == B.KV_ERR_NOT_FOUND
+    with pytest.raises(B.KVError) as e:
+        B.kv_evict_order(h, [r], [float("nan")])
+    assert e.value.code == B.KV_ERR_INVALID_ARG
+    with pytest.raises(B.KVError) as e:
+        B.kv_pool_create(8, 1, 1, 64, None, None, [0, 1, 2, 3, 4, 5, 6, 6])
+    assert e.value.code == B.KV_ERR_INVALID_ARG
+    B.kv_pool_destroy(h)
+
+
+def test_evict_order_matches_oracle():
+    w = W.deep_tree()
+    lib = H.Cache(w, with_data=False, evict=False)
+    ref = rp.replay(w, with_data=False)
+    cand = w.evict_candidates()
+    scores = [w.evict_scores[i] for i in cand]
+    assert B.kv_evict_order(lib.h, cand, scores) == \
+        ref.model.evict_order(cand, scores)
+
+
+# ---- batch builder --------------------------------------------------------------
+
+def test_tiny_tree_has_one_segment():
+    lib = H.Cache(W.tiny_tree(), with_data=False)
+    tables, lens, groups = B.kv_build_batch(lib.h, lib.decode_ids)
+    assert lens.tolist() == [120, 127, 133, 140]
+    assert groups.tolist() == [[0, 4, 0, 6]]
+    assert (tables[0, 8:] == -1).all()       # 120 tokens = 8 blocks
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_segments_are_valid_and_maximal(name):
+    w = SMALL[name]()
+    lib = H.Cache(w, with_data=False)
+    tables, lens, groups = B.kv_build_batch(lib.h, lib.decode_ids)
+    tl = [row[row >= 0].tolist() for row in tables]
+    att.validate_prefix_groups(groups, tl, lens, 16)
+    # Maximal: consecutive rows never share a full block beyond their
+    # deepest common segment.
+    ends = np.zeros(len(lens), dtype=int)
+    for bb, bc, kb, kc in groups:
+        ends[bb:bb + bc] = np.maximum(ends[bb:bb + bc], kb + kc)
+    for i in range(len(lens) - 1):
+        lim = min(lens[i], lens[i + 1]) // 16
+        j = 0
+        while j < lim and tl[i][j] == tl[i + 1][j]:
+            j += 1
+        assert min(ends[i], ends[i + 1]) >= j
+    if name == "fanout":
+        assert groups.tolist() == [[64 * r, 64, 0, 128] for r in range(8)]
+    if name == "long_context":
+        assert groups.tolist() == [[128 + 16 * r, 16, 0, 2048]
+                                   for r in range(16)]
+    if name == "independent":
+        assert len(groups) == 0
+
+
+# ---- decode plan ----------------------------------------------------------------
+
+def decode_plan(plan, info, nb, Hq, Hkv):
+    """Read the plan format documented in csrc/internal.h."""
+    hdr = plan[:16]
+    assert hdr[0] == 0x31564B50
+    nr, nt = int(hdr[5]), int(hdr[6])
+    rows = plan[int(hdr[8]):int(hdr[8]) + 8 * nr].reshape(-1, 8)
+    tiles = plan[int(hdr[9]):int(hdr[9]) + 8 * nt].reshape(-1, 8)
+    ptr = plan[int(hdr[10]):int(hdr[10]) + nb + 1]
+    ent = plan[int(hdr[11]):int(hdr[11]) + 4 * int(hdr[7])].reshape(-1, 4)
+    return rows, tiles, ptr, ent
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("flags", [0, B.KV_PLAN_IGNORE_GROUPS])
+def test_plan_covers_every_token_once(name, flags):
+    w = SMALL[name]()
+    lib = H.Cache(w, with_data=False)
+    bt = lib.batch(flags=flags, num_sms=152)
+    nb, G = bt.nb, w.Hq // w.Hkv
+    rows, tiles, ptr, ent = decode_plan(bt.plan, bt.info, nb, w.Hq, w.Hkv)
+    nblk = (bt.seq_lens + 15) // 16
+    # cover[b][g] counts how often each logical block is read for each row.
+    cover = {}
+    written = np.zeros(bt.info.partial_rows, dtype=int)
+    for it in np.concatenate([rows, tiles]):
+        b0, g, row0, nr, lo, hi, pbase, masked = [int(x) for x in it]
+        assert 0 <= lo < hi <= nblk[b0]
+        written[pbase:pbase + nr] += 1
+        for r in range(row0, row0 + nr):
+            b, qr = b0 + r // G, r % G
+            key = (b, g, qr)
+            cover.setdefault(key, np.zeros(nblk[b], dtype=int))
+            cover[key][lo:hi] += 1
+    assert (written == 1).all()
+    for b in range(nb):
+        for g in range(w.Hkv):
+            for qr in range(G):
+                assert (cover[(b, g, qr)] == 1).all()
+    # The merge list of each (branch, q-head) names one partial row per item
+    # covering it, and those rows' item covers that branch.
+    row_owner = {}
+    for it in np.concatenate([rows, tiles]):
+        b0, g, row0, nr, lo, hi, pbase, masked = [int(x) for x in it]
+        for r in range(nr):
+            row_owner[pbase + r] = (b0 + (row0 + r) // G, g, (row0 + r) % G,
+                                    hi - lo)
+    for b in range(nb):
+        for h in range(w.Hq):
+            g, qr = h // G, h % G
+            total = 0
+            for base, stride, lo, hi in ent[ptr[b]:ptr[b + 1]]:
+                if lo <= qr < hi:
+                    owner = row_owner[int(base + g * stride + qr - lo)]
+                    assert owner[:3] == (b, g, qr)
+                    total += owner[3]
+            assert total == nblk[b]
+    if flags & B.KV_PLAN_IGNORE_GROUPS:
+        assert (rows[:, 7] == 1).all()
+
+
+def test_plan_rejects_bad_input():
+    with pytest.raises(B.KVError):
+        B.paged_decode_plan(2, 8, 2, 128, 4, [10, 0], [])
+    with pytest.raises(B.KVError):
+        B.paged_decode_plan(2, 8, 2, 128, 4, [10, 80], [])        # > 4 blocks
+    with pytest.raises(B.KVError):      # segment block not full for row 0
+        B.paged_decode_plan(2, 8, 2, 128, 4, [20, 40], [[0, 2, 0, 2]])
+    with pytest.raises(B.KVError):      # gap: row's segments start at 1
+        B.paged_decode_plan(2, 8, 2, 128, 4, [40, 40], [[0, 2, 1, 1]])
+    with pytest.raises(B.KVError):      # overlap
+        B.paged_decode_plan(2, 8, 2, 128, 4, [40, 40],
+                            [[0, 2, 0, 2], [0, 2, 1, 1]])
+    plan, info = B.paged_decode_plan(2, 8, 2, 128, 4, [40, 40], [[0, 2, 0, 2]])
+    assert info.partial_rows > 0 and len(plan) == info.plan_ints
