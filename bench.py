@@ -119,7 +119,7 @@ def item_bytes(plan, info, Hkv, d, seq_lens, which):
         if masked:
             toks = min(toks, int(seq_lens[b0]) - 16 * lo)
         tot += toks
-    return tot * 2 * d * 2
+    return int(tot) * 2 * d * 2
 
 
 class ClockSampler:
@@ -284,6 +284,12 @@ def run_ours(args):
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)]
            for _ in range(K)]
+    # torch creates the CUDA event behind an Event on its first record: do
+    # that now, outside the timed region, so the library gets real handles.
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     if ws > 1:
@@ -475,7 +481,8 @@ def main():
     args = parse()
     res = run_reference(args) if args.impl == "reference" else run_ours(args)
     if res is not None:
-        print(json.dumps(res), flush=True)
+        print(json.dumps(res, default=lambda o: o.item() if hasattr(o, "item")
+                         else str(o)), flush=True)
 
 
 if __name__ == "__main__":

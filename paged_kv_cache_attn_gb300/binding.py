@@ -361,7 +361,10 @@ def kv_set_launch_events(events):
         _events_keepalive = None
         _check(_lib.kv_set_launch_events(None, 0))
         return
-    arr = (_vp * len(events))(*[e.cuda_event if e is not None else None
-                                for e in events])
+    handles = [e.cuda_event if e is not None else None for e in events]
+    if any(e is not None and not h for e, h in zip(events, handles)):
+        raise ValueError("record each torch.cuda.Event once before passing it "
+                         "(torch creates the CUDA event on first record)")
+    arr = (_vp * len(events))(*handles)
     _events_keepalive = arr
     _check(_lib.kv_set_launch_events(arr, len(events)))

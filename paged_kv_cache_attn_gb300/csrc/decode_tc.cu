@@ -1,12 +1,450 @@
-// tcgen05 kernel for 128-row shared-prefix tiles (not built yet: the plan
-// routes every segment to the split-KV kernel while kTensorCoreKernel is off).
+// Shared-prefix tile kernel on the 5th-generation tensor cores (tcgen05).
+//
+// One CTA = one tile item: 128 query rows of a shared-prefix segment (the
+// branches x GQA heads that share the segment's blocks, stacked as M) x one
+// kv-head x a range of the segment's logical blocks.  Every block of the
+// range is read from HBM once for all 128 rows -- the cross-branch re-read
+// that paging removes ("Dismantling the Memory Wall", copy-on-write section;
+// RKSC summary §1.1 on cross-branch KV waste) -- and the contraction is dense
+// enough (up to 128 flops per KV byte) to belong on the tensor cores.
+//
+// Pipeline per 64-token KV tile j (4 blocks of 16):
+//   warp 4  (TMA):     8 boxes of K and 8 of V (16 rows x 64 cols, 128-byte
+//                      swizzle) into stage j % 3 -> kv_full
+//   warp 5  (MMA):     S[j%2] = Q K^T  (M=128, N=64, K=128; TMEM, fp32)
+//                      -> s_full; then O += P(j-1) V(j-1) (M=128, N=128,
+//                      K=64; V as an MN-major operand) -> kv_empty, pv_done
+//   warps 0-3 (rows):  thread r owns row r: S row from TMEM, base-2 online
+//                      softmax with a lazy maximum (O and l are rescaled only
+//                      when the row maximum grows by more than 8, so p <= 256),
+//                      P row (bf16) into 128B-swizzled shared memory -> p_full
+// At the end the rows read O from TMEM and write unnormalised partials
+// (o, m, l), merged with the other passes by log-sum-exp.
+//
+// Tokens of a tile past the item's range come from TMA loads at an
+// out-of-range row (zero fill) and are masked out of the softmax.
+
 #include "device_common.cuh"
 
 namespace pkv {
-struct SplitParams;
-cudaError_t launch_tile_items(const CUtensorMap&, const CUtensorMap&,
-                              const SplitParams&, const WorkItem*, int, int,
-                              cudaStream_t) {
-  return cudaErrorNotSupported;
+namespace tc {
+
+constexpr int kT = 64;                   // tokens per KV tile
+constexpr int kTB = kT / 16;             // blocks per KV tile
+constexpr int kNS = 3;                   // KV stages
+constexpr int kBox = kT * 128;           // one 64-column box of a K/V tile
+constexpr int kKV = 2 * kBox;            // K (or V) tile, head_dim 128
+constexpr int kStage = 2 * kKV;          // K + V
+constexpr int kQBytes = 2 * 128 * 128;   // Q: 2 boxes x 128 rows x 128 B
+constexpr int kPBytes = 128 * kT * 2;    // P: 128 rows x 64 tokens bf16
+constexpr int kSmem = kQBytes + 2 * kPBytes + kNS * kStage + 1024;
+constexpr int kThreads = 192;            // warps 0-3 rows, 4 TMA, 5 MMA
+constexpr uint32_t kTmemCols = 256;      // S[0] 0..63, S[1] 64..127, O 128..255
+constexpr float kRescale = 8.f;          // lazy-max threshold (log2 units)
+
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 format: start
+// address >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride byte
+// offset >> 4 in 32-45, version 1 in 46-47, layout type 2 in 61-63).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo,
+                                          uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) |
+         ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
+         (2ull << 61);
 }
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A
+// K-major, B K-major or MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc(int M, int N, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b,
+                                     uint32_t id, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          tmem_d),
+      "l"(a), "l"(b), "r"(id), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
+      "[%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+#define PKV_R32(a)                                                           \
+  "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]),    \
+      "=r"(a[6]), "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]),           \
+      "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),       \
+      "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]),       \
+      "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]), "=r"(a[25]),       \
+      "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]),       \
+      "=r"(a[31])
+#define PKV_W32(a)                                                           \
+  "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]),          \
+      "r"(a[6]), "r"(a[7]), "r"(a[8]), "r"(a[9]), "r"(a[10]), "r"(a[11]),    \
+      "r"(a[12]), "r"(a[13]), "r"(a[14]), "r"(a[15]), "r"(a[16]),            \
+      "r"(a[17]), "r"(a[18]), "r"(a[19]), "r"(a[20]), "r"(a[21]),            \
+      "r"(a[22]), "r"(a[23]), "r"(a[24]), "r"(a[25]), "r"(a[26]),            \
+      "r"(a[27]), "r"(a[28]), "r"(a[29]), "r"(a[30]), "r"(a[31])
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, "
+      "[%32];"
+      : PKV_R32(v)
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr,
+                                          const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
+      PKV_W32(v)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a,
+                                             uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a),
+               "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+struct Bars {
+  uint64_t kv_full[kNS], kv_empty[kNS], s_full[2], p_full[2], pv_done[2],
+      o_ready, drain;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tile_decode_kernel(const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV,
+                       const SplitParams p, const WorkItem* items,
+                       int64_t oob_row) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) Bars bars;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = base;
+  const uint32_t sP = base + kQBytes;              // P[0], P[1]
+  const uint32_t sKV = sP + 2 * kPBytes;           // stages
+  const WorkItem it = items[blockIdx.x];
+  if (!item_ok(it, p, 128)) {
+    if (threadIdx.x == 0)
+      record_status(p.status, KV_ERR_DEVICE, -1 - (int)blockIdx.x);
+    return;
+  }
+  const int nblk = it.blk_end - it.blk_begin;
+  const int ntile = (nblk + kTB - 1) / kTB;
+  const int32_t* table = p.tables + (int64_t)it.branch0 * p.max_blocks;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(smem_u32(&bars.kv_full[s]), 1);
+      mbar_init(smem_u32(&bars.kv_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bars.s_full[b]), 1);
+      mbar_init(smem_u32(&bars.p_full[b]), 4);
+      mbar_init(smem_u32(&bars.pv_done[b]), 1);
+    }
+    mbar_init(smem_u32(&bars.o_ready), 1);
+    mbar_init(smem_u32(&bars.drain), 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    asm volatile(
+        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::
+            "r"(smem_u32(&tmem_base_sh)),
+        "r"(kTmemCols)
+        : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::
+                     : "memory");
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  // Q tile: row r = (branch, q-head) of the segment, 128B-swizzled K-major.
+  if (threadIdx.x < 128) {
+    const int r = threadIdx.x;
+    const uint4* src = nullptr;
+    if (r < it.nrows) {
+      const int rr = it.row0 + r;
+      const int b = it.branch0 + rr / p.G;
+      const int qh = it.g * p.G + rr % p.G;
+      src = reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.Hq + qh) * 128);
+    }
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 v = src ? src[c] : make_uint4(0, 0, 0, 0);
+      const uint32_t a = sQ + (c >> 3) * 16384 + r * 128 +
+                         (((c & 7) ^ (r & 7)) << 4);
+      st_shared_v4(a, v.x, v.y, v.z, v.w);
+    }
+    fence_proxy_async_smem();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 4) {
+    // ---- TMA producer ----------------------------------------------------
+    if (lane == 0) {
+      int issued = 0;
+      for (int j = 0; j < ntile; ++j) {
+        const int s = j % kNS;
+        if (j >= kNS &&
+            !mbar_wait(smem_u32(&bars.kv_empty[s]), ((j / kNS) - 1) & 1)) {
+          record_status(p.status, KV_ERR_TIMEOUT, 10);
+          atomicExch(&abort_sh, 1);
+        }
+        if (*(volatile int*)&abort_sh) break;
+        const uint32_t fb = smem_u32(&bars.kv_full[s]);
+        mbar_expect_tx(fb, kStage);
+        const uint32_t kst = sKV + s * kStage, vst = kst + kKV;
+        for (int i = 0; i < kTB; ++i) {
+          const int jb = it.blk_begin + j * kTB + i;
+          int64_t y = oob_row;  // zero fill past the range
+          if (jb < it.blk_end) {
+            const int phys = table[jb];
+            if (phys >= 0 && (int64_t)phys < p.num_blocks)
+              y = ((int64_t)phys * p.Hkv + it.g) * 16;
+            else
+              record_status(p.status, KV_ERR_DEVICE, phys);
+          }
+          for (int bx = 0; bx < 2; ++bx) {
+            tma_load_2d(kst + bx * kBox + i * 2048, &tmK, bx * 64, (int)y, fb);
+            tma_load_2d(vst + bx * kBox + i * 2048, &tmV, bx * 64, (int)y, fb);
+          }
+        }
+        issued = j + 1;
+      }
+      // Let every load this CTA issued land before it can exit.
+      const int first = issued > kNS ? issued - kNS : 0;
+      for (int j = first; j < issued; ++j)
+        mbar_wait(smem_u32(&bars.kv_full[j % kNS]), (j / kNS) & 1);
+    }
+  } else if (warp == 5) {
+    // ---- MMA issuer ------------------------------------------------------
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc(128, kT, false);
+      constexpr uint32_t id_pv = idesc(128, 128, true);
+      bool ok = true;
+      auto pv = [&](int jp) {
+        const int b = jp & 1, s = jp % kNS;
+        if (!mbar_wait(smem_u32(&bars.p_full[b]), (jp >> 1) & 1)) return false;
+        fence_after_sync();
+        const uint32_t vst = sKV + s * kStage + kKV;
+#pragma unroll
+        for (int kt = 0; kt < kT / 16; ++kt) {
+          const uint64_t a = sdesc(sP + b * kPBytes + kt * 32, 16, 1024);
+          const uint64_t bd = sdesc(vst + kt * 2048, kBox, 1024);
+          umma(tmem + 128, a, bd, id_pv, (jp > 0 || kt > 0) ? 1u : 0u);
+        }
+        umma_commit(smem_u32(&bars.kv_empty[s]));
+        umma_commit(smem_u32(&bars.pv_done[b]));
+        return true;
+      };
+      for (int j = 0; j < ntile && ok; ++j) {
+        const int s = j % kNS, b = j & 1;
+        if (!mbar_wait(smem_u32(&bars.kv_full[s]), (j / kNS) & 1)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        const uint32_t kst = sKV + s * kStage;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = sdesc(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16,
+                                   1024);
+          const uint64_t bd = sdesc(kst + (kk >> 2) * kBox + (kk & 3) * 32, 16,
+                                    1024);
+          umma(tmem + b * kT, a, bd, id_qk, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(smem_u32(&bars.s_full[b]));
+        if (j >= 1) ok = pv(j - 1);
+      }
+      if (ok) ok = pv(ntile - 1);
+      if (!ok) {
+        record_status(p.status, KV_ERR_TIMEOUT, 11);
+        atomicExch(&abort_sh, 1);
+      }
+      umma_commit(smem_u32(&bars.o_ready));
+      // Drain: every MMA this thread issued has finished once this lands.
+      umma_commit(smem_u32(&bars.drain));
+      mbar_wait(smem_u32(&bars.drain), 0);
+    }
+  } else {
+    // ---- softmax rows (warps 0-3; thread r <-> TMEM lane r) ----------------
+    const int r = threadIdx.x;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntile; ++j) {
+      const int b = j & 1;
+      if (!mbar_wait(smem_u32(&bars.s_full[b]), (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      fence_after_sync();
+      uint32_t sv[2][32];
+      tmem_ld32(lane_base + b * kT, sv[0]);
+      tmem_ld32(lane_base + b * kT + 32, sv[1]);
+      tmem_wait_ld();
+      const int valid = min(kT, (it.blk_end - (it.blk_begin + j * kTB)) * 16);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (h * 32 + c < valid) mx = fmaxf(mx, __uint_as_float(sv[h][c]));
+      const float m_tile = mx * p.scale_log2;
+      const bool need = m_tile > m_used + kRescale;
+      const float m_new = need ? m_tile : m_used;
+      const float alpha = need ? ex2(m_used - m_new) : 1.f;
+      if (__any_sync(0xffffffffu, need) && j > 0) {
+        // O holds PV up to tile j-1: wait for it, then rescale this row.
+        if (!mbar_wait(smem_u32(&bars.pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(lane_base + 128 + c * 32, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st32(lane_base + 128 + c * 32, ov);
+        }
+        tmem_wait_st();
+      }
+      l *= alpha;
+      m_used = m_new;
+      // P row (bf16) for this tile.
+      if (j >= 2 &&
+          !mbar_wait(smem_u32(&bars.pv_done[b]), ((j - 2) >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const uint32_t prow = sP + b * kPBytes + r * 128;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c0 = ch * 8 + 2 * e;
+          const float s0 = __uint_as_float(sv[c0 >> 5][c0 & 31]);
+          const float s1 = __uint_as_float(sv[(c0 + 1) >> 5][(c0 + 1) & 31]);
+          const float p0 = c0 < valid ? ex2(s0 * p.scale_log2 - m_used) : 0.f;
+          const float p1 =
+              c0 + 1 < valid ? ex2(s1 * p.scale_log2 - m_used) : 0.f;
+          l += p0 + p1;
+          w4[e] = pack_bf16(p0, p1);
+        }
+        st_shared_v4(prow + ((ch ^ (r & 7)) << 4), w4[0], w4[1], w4[2], w4[3]);
+      }
+      fence_proxy_async_smem();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[b]));
+    }
+    if (!ok) {
+      if (lane == 0) record_status(p.status, KV_ERR_TIMEOUT, 12);
+      atomicExch(&abort_sh, 1);
+    }
+    // Epilogue: O row from TMEM -> unnormalised partial row.
+    const bool done = mbar_wait(smem_u32(&bars.o_ready), 0);
+    fence_after_sync();
+    // tcgen05.ld is warp-collective: decide once per warp.
+    if (__all_sync(0xffffffffu,
+                   done && ok && !*(volatile int*)&abort_sh)) {
+      float* dst = p.o + (int64_t)(it.prow_base + r) * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(lane_base + 128 + c * 32, ov);
+        tmem_wait_ld();
+        if (r < it.nrows) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(dst + c * 32 + i) =
+                make_float4(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1]),
+                            __uint_as_float(ov[i + 2]),
+                            __uint_as_float(ov[i + 3]));
+        }
+      }
+      if (r < it.nrows) p.ml[it.prow_base + r] = make_float2(m_used, l);
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 5) {
+    asm volatile(
+        "tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+        "r"(kTmemCols)
+        : "memory");
+  }
+}
+
+}  // namespace tc
+
+cudaError_t launch_tile_items(const CUtensorMap& tk, const CUtensorMap& tv,
+                              const SplitParams& sp, const WorkItem* items,
+                              int n_items, int d, cudaStream_t stream) {
+  if (d != 128) return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(
+        tc::tile_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        tc::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  // A row past the end of the pool's 2-D view: TMA fills the box with zeros.
+  const int64_t oob_row = sp.num_blocks * sp.Hkv * 16;
+  tc::tile_decode_kernel<<<n_items, tc::kThreads, tc::kSmem, stream>>>(
+      tk, tv, sp, items, oob_row);
+  return cudaGetLastError();
+}
+
 }  // namespace pkv

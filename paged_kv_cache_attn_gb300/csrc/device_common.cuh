@@ -129,4 +129,32 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
                : "memory");
 }
 
+// Arguments shared by the attention kernels (one launch, one layer).
+struct SplitParams {
+  const __nv_bfloat16* q;
+  const int32_t* tables;
+  const int32_t* seq_lens;
+  const WorkItem* items;
+  float2* ml;
+  float* o;
+  DeviceStatus* status;
+  int nb, Hq, Hkv, G, max_blocks;
+  int64_t num_blocks;
+  int64_t partial_rows;
+  float scale_log2;
+};
+
+// A work item read from the (caller-uploaded) plan must stay inside the
+// arrays it indexes; a malformed one is recorded and skipped.
+__device__ __forceinline__ bool item_ok(const WorkItem& it,
+                                        const SplitParams& p, int max_rows) {
+  const int64_t last_row = (int64_t)it.row0 + it.nrows - 1;
+  return it.nrows >= 1 && it.nrows <= max_rows && it.row0 >= 0 &&
+         it.branch0 >= 0 && it.branch0 + last_row / p.G < p.nb &&
+         it.g >= 0 && it.g < p.Hkv && it.blk_begin >= 0 &&
+         it.blk_begin < it.blk_end && it.blk_end <= p.max_blocks &&
+         it.prow_base >= 0 &&
+         (int64_t)it.prow_base + it.nrows <= p.partial_rows;
+}
+
 }  // namespace pkv

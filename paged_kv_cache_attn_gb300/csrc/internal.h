@@ -43,7 +43,7 @@ struct MergeEntry {
   int32_t base, stride, r_lo, r_hi;
 };
 
-constexpr bool kTensorCoreKernel = false;  // tcgen05 tile kernel available
+constexpr bool kTensorCoreKernel = true;  // tcgen05 tile kernel available
 constexpr int kTileRows = 128;      // rows of a tcgen05 tile
 constexpr int kRowTile = 16;        // rows of an mma.sync tile
 constexpr int kMinTensorRows = 65;  // segments with more rows go to tcgen05

@@ -77,8 +77,9 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   std::vector<int32_t> shared_end(nb, 0);
   std::vector<Unit> units;
   const bool use_groups = !(flags & KV_PLAN_IGNORE_GROUPS);
-  const bool allow_tc =
-      pkv::kTensorCoreKernel && !(flags & KV_PLAN_NO_TENSOR_CORES);
+  // The tcgen05 tile kernel is built for head_dim 128.
+  const bool allow_tc = pkv::kTensorCoreKernel && d == 128 &&
+                        !(flags & KV_PLAN_NO_TENSOR_CORES);
   if (use_groups && n_groups > 0) {
     std::vector<std::vector<std::pair<int32_t, int32_t>>> per_row(nb);
     for (int32_t i = 0; i < n_groups; ++i) {
