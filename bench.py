@@ -263,7 +263,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     dev = f"cuda:{local if ws > 1 else 0}"
     torch.cuda.set_device(dev)
-    w = W.CONFIGS[args.workload]()
+    w = W.make(args.workload, rank)
     cache = H.Cache(w, device=dev)
     bt = cache.batch().upload()
     nb = bt.nb

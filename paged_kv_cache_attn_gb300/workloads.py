@@ -246,3 +246,14 @@ CONFIGS = {
     "deep_tree": deep_tree,
     "long_context": long_context,
 }
+
+
+def make(name: str, rank: int = 0, **sizes) -> Workload:
+    """Workload ``name`` for one rank of a multi-GPU run.  Every rank gets its
+    own trees (the default seed offset by 1000 x rank) of the same shape, so
+    ranks share nothing and need no exchange."""
+    import inspect
+    fn = CONFIGS[name]
+    seed = inspect.signature(fn).parameters["seed"].default + 1000 * rank
+    return fn(seed=seed, **sizes)
+
