@@ -270,6 +270,30 @@ kv_status paged_decode_attn(const void* q, const void* k_pool,
                             const kv_decode_plan_info* info, void* workspace,
                             size_t ws_bytes, void* stream);
 
+/* paged_decode_attn without a caller workspace.  The pages have no
+ * counterpart: this exists for callers that cannot allocate device memory
+ * (a plug-in whose host engine owns every device buffer and offers it no
+ * allocator, a process that reserved the whole GPU at start-up, a
+ * latency-critical path that cannot pay for cudaMalloc or its implicit
+ * synchronisation).  Same arguments, meaning and errors as paged_decode_attn
+ * minus workspace / ws_bytes: the step's scratch (status word and partial
+ * results) lives in a library-owned __device__ array of 64 MiB that every GPU
+ * loading the library holds until the process exits.  A step whose
+ * info->workspace_bytes exceeds 64 MiB is rejected with INVALID_ARG.  The
+ * first call on a device looks up the array's device address (with that
+ * device current) and should come before any stream capture.  All calls share
+ * the array and it keeps the last call's contents; each call clears the part
+ * that must start at zero; calls whose work overlaps on the GPU race.  Kernel
+ * status recorded in this scratch is not readable by kv_check_device_status.
+ * Calls no cudaMalloc, cudaFree or other allocating routine. */
+kv_status paged_decode_attn_noalloc(
+    const void* q, const void* k_pool, const void* v_pool, int64_t num_blocks,
+    const int32_t* block_tables, const int32_t* seq_lens,
+    const int32_t* prefix_groups, int32_t n_groups, int32_t nb,
+    int32_t max_blocks, int32_t Hq, int32_t Hkv, int32_t head_dim,
+    int32_t block_size, float scale, void* out, const int32_t* plan,
+    const kv_decode_plan_info* info, void* stream);
+
 /* Read (synchronising `stream`) and clear the status word of a workspace used
  * by paged_decode_attn.  *out_code: 0, KV_ERR_DEVICE or KV_ERR_TIMEOUT;
  * *out_detail (nullable): the first bad value recorded.  Errors: CUDA. */

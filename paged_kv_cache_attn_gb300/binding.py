@@ -106,6 +106,13 @@ _SIGS = {
                                       C.c_int32, C.c_float, _vp, _vp,
                                       C.POINTER(kv_decode_plan_info), _vp,
                                       C.c_size_t, _vp]),
+    "paged_decode_attn_noalloc": (C.c_int32, [_vp, _vp, _vp, C.c_int64, _vp,
+                                              _vp, _vp, C.c_int32, C.c_int32,
+                                              C.c_int32, C.c_int32, C.c_int32,
+                                              C.c_int32, C.c_int32, C.c_float,
+                                              _vp, _vp,
+                                              C.POINTER(kv_decode_plan_info),
+                                              _vp]),
     "kv_check_device_status": (C.c_int32, [_vp, _vp, _i32p, _i32p]),
     "kv_set_launch_events": (C.c_int32, [C.POINTER(_vp), C.c_int32]),
     "kv_last_error": (C.c_char_p, []),
@@ -340,6 +347,18 @@ def paged_decode_attn(q, k_pool, v_pool, num_blocks, block_tables, seq_lens,
         _ptr(seq_lens), _ptr(prefix_groups), n_groups, nb, max_blocks, Hq, Hkv,
         head_dim, block_size, scale, _ptr(out), _ptr(plan), C.byref(info),
         _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def paged_decode_attn_noalloc(q, k_pool, v_pool, num_blocks, block_tables,
+                              seq_lens, prefix_groups, n_groups, nb,
+                              max_blocks, Hq, Hkv, head_dim, scale, out, plan,
+                              info, stream=None, block_size=16):
+    """paged_decode_attn with the library's built-in scratch (no workspace)."""
+    _check(_lib.paged_decode_attn_noalloc(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), num_blocks, _ptr(block_tables),
+        _ptr(seq_lens), _ptr(prefix_groups), n_groups, nb, max_blocks, Hq, Hkv,
+        head_dim, block_size, scale, _ptr(out), _ptr(plan), C.byref(info),
+        _stream(stream)))
 
 
 def kv_check_device_status(workspace, stream=None):
