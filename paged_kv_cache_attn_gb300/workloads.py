@@ -239,12 +239,20 @@ def long_context(seed: int = 1005, n_indep: int = 128, indep_tokens: int = 8192,
     return _finish(w)
 
 
+def long_context_quarter(seed: int = 1005) -> Workload:
+    """long_context at a quarter of the trees (for profiler captures)."""
+    w = long_context(seed=seed, n_indep=32, n_roots=4)
+    w.name = "long_context_quarter"
+    return w
+
+
 CONFIGS = {
     "tiny_tree": tiny_tree,
     "independent": independent,
     "fanout": fanout,
     "deep_tree": deep_tree,
     "long_context": long_context,
+    "long_context_quarter": long_context_quarter,
 }
 
 
