@@ -336,38 +336,53 @@ def run_ours(args):
              "tile_tcgen05": "tile_decode_kernel"}[dom]
     traffic = traffic_per_launch(kname, w.name)
 
-    # End to end through the public API with host buffers: per step, build the
-    # batch and plan on the host, copy q / tables / lengths / segments / plan
-    # host -> device from pinned memory, run the step, copy out back.
-    q_pin = torch.from_numpy(q_host.view(np.int16)).pin_memory()
-    out_pin = torch.empty((nb, w.Hq, w.d), dtype=torch.int16).pin_memory()
+    # End to end through the public API with host buffers: per step the host
+    # builds the batch and the plan into pinned staging buffers (allocated
+    # once, as an engine would), copies q / tables / lengths / segments / plan
+    # host -> device, runs the step and copies the output back.
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    e2e_t, h2d, d2h = [], 0, 0
+    mb = bt.tables.shape[1]
+    pin = {
+        "q": torch.from_numpy(q_host.view(np.int16)).pin_memory(),
+        "tables": torch.empty((nb, mb), dtype=torch.int32).pin_memory(),
+        "lens": torch.empty(nb, dtype=torch.int32).pin_memory(),
+        "groups": torch.empty((nb + 1) * 4, dtype=torch.int32).pin_memory(),
+        "plan": torch.empty(2 * len(bt.plan) + 1024,
+                            dtype=torch.int32).pin_memory(),
+        "out": torch.empty((nb, w.Hq, w.d), dtype=torch.int16).pin_memory(),
+    }
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in pin.items()
+            if k != "out"}
+    wsb = torch.empty(2 * bt.info.workspace_bytes + 4096, dtype=torch.uint8,
+                      device=dev)
+    e2e_t = []
+    h2d = d2h = 0
     for i in range(args.e2e_steps + 3):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        tables, lens, groups = B.kv_build_batch(cache.h, bt.ids)
-        plan, info = B.paged_decode_plan(nb, w.Hq, w.Hkv, w.d,
-                                         tables.shape[1], lens, groups, sms)
-        host = [torch.from_numpy(a).pin_memory() for a in
-                (tables, lens, groups.reshape(-1) if len(groups)
-                 else np.zeros(4, np.int32), plan)]
-        devs = [x.to(dev, non_blocking=True) for x in host]
-        qd = q_pin.to(dev, non_blocking=True).view(torch.bfloat16)
-        wsb = bt.dev["workspace"]
-        if wsb.numel() < info.workspace_bytes:
-            wsb = torch.empty(info.workspace_bytes, dtype=torch.uint8, device=dev)
-        B.paged_decode_attn(qd, cache.k[0], cache.v[0], w.num_blocks, devs[0],
-                            devs[1], devs[2], len(groups), nb, tables.shape[1],
-                            w.Hq, w.Hkv, w.d, w.scale, out, devs[3], info, wsb,
-                            wsb.numel())
-        out_pin.copy_(out.view(torch.int16), non_blocking=True)
+        tables, lens, groups = B.kv_build_batch(
+            cache.h, bt.ids, mb, pin["tables"].numpy(), pin["lens"].numpy(),
+            pin["groups"].numpy())
+        plan, info = B.paged_decode_plan(nb, w.Hq, w.Hkv, w.d, mb, lens,
+                                         groups, sms,
+                                         plan_out=pin["plan"].numpy())
+        n_g = 4 * max(len(groups), 1)
+        parts = [("q", pin["q"].numel()), ("tables", nb * mb), ("lens", nb),
+                 ("groups", n_g), ("plan", len(plan))]
+        for k, n in parts:
+            dbuf[k][:n].copy_(pin[k][:n], non_blocking=True) if \
+                dbuf[k].dim() == 1 else dbuf[k].copy_(pin[k], non_blocking=True)
+        qd = dbuf["q"].view(torch.bfloat16)
+        B.paged_decode_attn(qd, cache.k[0], cache.v[0], w.num_blocks,
+                            dbuf["tables"], dbuf["lens"], dbuf["groups"],
+                            len(groups), nb, mb, w.Hq, w.Hkv, w.d, w.scale,
+                            out, dbuf["plan"], info, wsb, wsb.numel())
+        pin["out"].copy_(out.view(torch.int16), non_blocking=True)
         torch.cuda.synchronize()
         if i >= 3:
             e2e_t.append(time.perf_counter() - t0)
-        h2d = sum(x.numel() * x.element_size() for x in host) + \
-            q_pin.numel() * q_pin.element_size()
-        d2h = out_pin.numel() * out_pin.element_size()
+        h2d = sum(n * 4 for _, n in parts[1:]) + pin["q"].numel() * 2
+        d2h = pin["out"].numel() * 2
     e2e_s = statistics.median(e2e_t)
 
     res = None

@@ -257,8 +257,8 @@ kv_status paged_decode_attn_workspace_size(const kv_decode_plan_info* info,
  * Error behaviour: argument errors return INVALID_ARG before any launch; a
  * block id outside [0, num_blocks) or a timed-out wait is recorded in the
  * workspace status word (the access is skipped, the output is then
- * unspecified) and reported by kv_check_device_status.  Errors: INVALID_ARG,
- * CUDA. */
+ * unspecified) and reported by kv_check_device_status.  scale must be finite
+ * and > 0.  Errors: INVALID_ARG, CUDA. */
 kv_status paged_decode_attn(const void* q, const void* k_pool,
                             const void* v_pool, int64_t num_blocks,
                             const int32_t* block_tables,

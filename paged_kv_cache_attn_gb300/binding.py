@@ -297,30 +297,51 @@ def kv_batch_max_blocks(h, ids) -> int:
     return out.value
 
 
-def kv_build_batch(h, ids, max_blocks=None):
-    """Host (tables [nb][max_blocks], seq_lens [nb], groups [ng][4])."""
+def kv_build_batch(h, ids, max_blocks=None, tables=None, seq_lens=None,
+                   groups=None):
+    """Host (tables [nb][max_blocks], seq_lens [nb], groups [ng][4]).
+
+    Optional output arrays (int32, C-contiguous; groups with >= nb rows of 4)
+    are filled in place -- e.g. numpy views of pinned staging buffers; the
+    returned groups is then a view of the filled rows."""
     ids = _i32(ids)
     nb = len(ids)
     if max_blocks is None:
         max_blocks = max(kv_batch_max_blocks(h, ids), 1)
-    tables = np.zeros((nb, max_blocks), dtype=np.int32)
-    lens = np.zeros(nb, dtype=np.int32)
-    cap = 2 * nb + 1
-    groups = np.zeros((cap, 4), dtype=np.int32)
+    if tables is None:
+        tables = np.zeros((nb, max_blocks), dtype=np.int32)
+    if seq_lens is None:
+        seq_lens = np.zeros(nb, dtype=np.int32)
+    fresh = groups is None
+    if fresh:
+        groups = np.zeros((nb + 1, 4), dtype=np.int32)
+    for a in (tables, seq_lens, groups):
+        assert a.dtype == np.int32 and a.flags.c_contiguous
+    assert tables.size >= nb * max_blocks and seq_lens.size >= nb
     ng = C.c_int32()
     _check(_lib.kv_build_batch(h, nb, _as_i32p(ids), max_blocks,
-                               _as_i32p(tables), _as_i32p(lens), cap,
-                               C.byref(ng), _as_i32p(groups)))
-    return tables, lens, groups[:ng.value].copy()
+                               _as_i32p(tables), _as_i32p(seq_lens),
+                               groups.size // 4, C.byref(ng),
+                               _as_i32p(groups)))
+    g = groups.reshape(-1, 4)[:ng.value]
+    return tables, seq_lens, (g.copy() if fresh else g)
 
 
 def paged_decode_plan(nb, Hq, Hkv, head_dim, max_blocks, seq_lens, groups,
-                      num_sms=0, flags=0, block_size=16):
-    """Host plan (int32 array) and its kv_decode_plan_info."""
+                      num_sms=0, flags=0, block_size=16, plan_out=None):
+    """Host plan (int32 array) and its kv_decode_plan_info.  With plan_out
+    (int32, large enough) the plan is written there and a view returned."""
     lens = _i32(seq_lens)
     g = _i32(groups).reshape(-1, 4)
     info = kv_decode_plan_info()
     gp = _as_i32p(g) if len(g) else None
+    if plan_out is not None:
+        assert plan_out.dtype == np.int32 and plan_out.flags.c_contiguous
+        _check(_lib.paged_decode_plan(nb, Hq, Hkv, head_dim, block_size,
+                                      max_blocks, _as_i32p(lens), gp, len(g),
+                                      num_sms, flags, _as_i32p(plan_out),
+                                      plan_out.size, C.byref(info)))
+        return plan_out[:info.plan_ints], info
     _check(_lib.paged_decode_plan(nb, Hq, Hkv, head_dim, block_size,
                                   max_blocks, _as_i32p(lens), gp, len(g),
                                   num_sms, flags, None, 0, C.byref(info)))

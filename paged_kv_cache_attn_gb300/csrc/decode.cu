@@ -9,9 +9,10 @@
 // Split-KV kernel (one CTA = one work item = up to 16 query rows x one
 // kv-head x a range of logical blocks):
 //  * 4 warps; warp w takes blocks w, w + 4, ... of the range.  Each warp runs
-//    its own NS-stage ring: lane 0 issues two 2-D TMA loads per 64 columns of
-//    the (block, kv-head) K and V tiles (16 rows x 128 B, 128-byte swizzle)
-//    completing on the stage's mbarrier; the whole warp waits on it.
+//    its own 3-stage ring (two CTAs fit on an SM): per block, lanes 0-3 each
+//    issue one 2-D TMA box (16 rows x 64 columns, 128-byte swizzle) of the
+//    (block, kv-head) K and V tiles, completing on the stage's mbarrier; the
+//    whole warp waits on it.
 //  * S = Q K^T with mma.sync m16n8k16: query rows are M (16), the block's
 //    16 tokens are N (two n8 tiles), head_dim is K.  The S accumulator layout
 //    is the A-operand layout of the next product, so P never leaves
@@ -49,7 +50,7 @@ struct SplitCfg {
 };
 
 template <int D, int NS>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(128, 2)
     splitkv_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV,
                           const SplitParams p) {
@@ -87,30 +88,39 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t ring = base + warp * NS * C::kStageBytes;
   const uint32_t bar0 = smem_u32(&bars[warp][0]);
 
+  // This warp's block-table entries, 32 at a time in registers (lane i holds
+  // the entry of the warp's (32 * window + i)-th block): one coalesced load
+  // per 32 blocks instead of a dependent load before every TMA issue.
+  int tcache = 0, twin = -1;
   // Issue the loads of this warp's k-th block into stage k % NS.  Returns
-  // whether the block id is inside the pool (uniform across the warp: every
-  // lane reads the same table entry).
+  // whether the block id is inside the pool (uniform across the warp).
   auto issue = [&](int k) -> bool {
-    const int j = it.blk_begin + warp + C::kWarps * k;
-    const int phys = table[j];
+    if ((k >> 5) != twin) {
+      twin = k >> 5;
+      const int kk = (twin << 5) + lane;
+      tcache = kk < my_n ? table[it.blk_begin + warp + C::kWarps * kk] : 0;
+    }
+    const int phys = __shfl_sync(0xffffffffu, tcache, k & 31);
     const bool ok = phys >= 0 && (int64_t)phys < p.num_blocks;
     const int s = k % NS;
     const uint32_t st = ring + s * C::kStageBytes;
     const uint32_t bar = bar0 + s * 8;
-    if (lane == 0) {
-      if (ok) {
-        fence_proxy_async_smem();
-        mbar_expect_tx(bar, C::kStageBytes);
+    if (ok) {
+      // Lane 0 arms the barrier; lanes 0 .. 2*kBoxes-1 then issue one box
+      // each in a single instruction (K and V, each kBoxes column halves).
+      fence_proxy_async_smem();
+      if (lane == 0) mbar_expect_tx(bar, C::kStageBytes);
+      __syncwarp();
+      if (lane < 2 * C::kBoxes) {
         const int y = (phys * p.Hkv + it.g) * 16;
-#pragma unroll
-        for (int bx = 0; bx < C::kBoxes; ++bx) {
-          tma_load_2d(st + bx * 2048, &tmK, bx * 64, y, bar);
-          tma_load_2d(st + C::kTileBytes + bx * 2048, &tmV, bx * 64, y, bar);
-        }
-      } else {
-        record_status(p.status, KV_ERR_DEVICE, phys);
-        mbar_arrive(bar);
+        const int bx = lane % C::kBoxes;
+        const bool is_v = lane >= C::kBoxes;
+        tma_load_2d(st + (is_v ? C::kTileBytes : 0) + bx * 2048,
+                    is_v ? &tmV : &tmK, bx * 64, y, bar);
       }
+    } else if (lane == 0) {
+      record_status(p.status, KV_ERR_DEVICE, phys);
+      mbar_arrive(bar);
     }
     return ok;
   };
@@ -392,7 +402,7 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const MergeParams p) {
 
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -504,7 +514,8 @@ extern "C" kv_status paged_decode_attn(
     return fail(KV_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned");
   if ((uintptr_t)workspace & 255)
     return fail(KV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-  if (!std::isfinite(scale)) return fail(KV_ERR_INVALID_ARG, "scale not finite");
+  if (!std::isfinite(scale) || !(scale > 0.f))
+    return fail(KV_ERR_INVALID_ARG, "scale must be finite and > 0");
   if (info->n_merge_rows != nb || info->partial_rows < 0)
     return fail(KV_ERR_INVALID_ARG, "plan info does not match nb");
   const size_t need = pkv::ws_total(info->partial_rows, d);

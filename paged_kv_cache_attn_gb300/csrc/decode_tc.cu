@@ -9,11 +9,13 @@
 // enough (up to 128 flops per KV byte) to belong on the tensor cores.
 //
 // Pipeline per 64-token KV tile j (4 blocks of 16):
-//   warp 4  (TMA):     8 boxes of K and 8 of V (16 rows x 64 cols, 128-byte
-//                      swizzle) into stage j % 3 -> kv_full
-//   warp 5  (MMA):     S[j%2] = Q K^T  (M=128, N=64, K=128; TMEM, fp32)
-//                      -> s_full; then O += P(j-1) V(j-1) (M=128, N=128,
-//                      K=64; V as an MN-major operand) -> kv_empty, pv_done
+//   warps 5-8 (TMA):   K and V, each as two column halves: 4 boxes (16 rows
+//                      x 64 cols, 128-byte swizzle) per warp and tile into
+//                      stage j % 4 -> k_full / v_full
+//   warp 4  (MMA):     S[j%2] = Q K^T  (M=128, N=64, K=128; TMEM, fp32)
+//                      -> s_full, k_empty; then O += P(j-1) V(j-1) (M=128,
+//                      N=128, K=64; V as an MN-major operand) -> v_empty,
+//                      pv_done
 //   warps 0-3 (rows):  thread r owns row r: S row from TMEM, base-2 online
 //                      softmax with a lazy maximum (O and l are rescaled only
 //                      when the row maximum grows by more than 8, so p <= 256),
@@ -31,16 +33,17 @@ namespace tc {
 
 constexpr int kT = 64;                   // tokens per KV tile
 constexpr int kTB = kT / 16;             // blocks per KV tile
-constexpr int kNS = 3;                   // KV stages
+constexpr int kNS = 4;                   // stages of each of the K and V rings
 constexpr int kBox = kT * 128;           // one 64-column box of a K/V tile
 constexpr int kKV = 2 * kBox;            // K (or V) tile, head_dim 128
-constexpr int kStage = 2 * kKV;          // K + V
 constexpr int kQBytes = 2 * 128 * 128;   // Q: 2 boxes x 128 rows x 128 B
 constexpr int kPBytes = 128 * kT * 2;    // P: 128 rows x 64 tokens bf16
-constexpr int kSmem = kQBytes + 2 * kPBytes + kNS * kStage + 1024;
-constexpr int kThreads = 192;            // warps 0-3 rows, 4 TMA, 5 MMA
+constexpr int kSmem = kQBytes + 2 * kPBytes + 2 * kNS * kKV + 1024;
+constexpr int kThreads = 288;            // warps 0-3 rows, 4 MMA, 5-8 TMA
+constexpr int kMmaWarp = 4;
 constexpr uint32_t kTmemCols = 256;      // S[0] 0..63, S[1] 64..127, O 128..255
 constexpr float kRescale = 8.f;          // lazy-max threshold (log2 units)
+constexpr int kTblWin = 128;             // block-table entries staged at once
 
 // Shared-memory matrix descriptor, 128-byte swizzle (sm_100 format: start
 // address >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride byte
@@ -141,8 +144,8 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a,
 }
 
 struct Bars {
-  uint64_t kv_full[kNS], kv_empty[kNS], s_full[2], p_full[2], pv_done[2],
-      o_ready, drain;
+  uint64_t k_full[kNS], k_empty[kNS], v_full[kNS], v_empty[kNS], s_full[2],
+      p_full[2], pv_done[2], o_ready, drain;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -154,13 +157,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) Bars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
+  __shared__ int tbl_sh[4][kTblWin];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = base;
   const uint32_t sP = base + kQBytes;              // P[0], P[1]
-  const uint32_t sKV = sP + 2 * kPBytes;           // stages
+  const uint32_t sK = sP + 2 * kPBytes;            // K ring
+  const uint32_t sV = sK + kNS * kKV;              // V ring
   const WorkItem it = items[blockIdx.x];
   if (!item_ok(it, p, 128)) {
     if (threadIdx.x == 0)
@@ -173,8 +178,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNS; ++s) {
-      mbar_init(smem_u32(&bars.kv_full[s]), 1);
-      mbar_init(smem_u32(&bars.kv_empty[s]), 1);
+      mbar_init(smem_u32(&bars.k_full[s]), 2);   // two K producer warps
+      mbar_init(smem_u32(&bars.k_empty[s]), 1);
+      mbar_init(smem_u32(&bars.v_full[s]), 2);   // two V producer warps
+      mbar_init(smem_u32(&bars.v_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bars.s_full[b]), 1);
@@ -186,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     abort_sh = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     asm volatile(
         "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::
             "r"(smem_u32(&tmem_base_sh)),
@@ -195,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::
                      : "memory");
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 5 && lane == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
@@ -223,44 +230,70 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp == 4) {
-    // ---- TMA producer ----------------------------------------------------
-    if (lane == 0) {
-      int issued = 0;
-      for (int j = 0; j < ntile; ++j) {
-        const int s = j % kNS;
-        if (j >= kNS &&
-            !mbar_wait(smem_u32(&bars.kv_empty[s]), ((j / kNS) - 1) & 1)) {
-          record_status(p.status, KV_ERR_TIMEOUT, 10);
-          atomicExch(&abort_sh, 1);
+  if (warp >= 5) {
+    // ---- TMA producers: warp 5 / 6 = K column half 0 / 1, warp 7 / 8 = V.
+    // Each issues its half of a tile's 4 blocks from lanes 0-3 in one
+    // instruction.  A single thread issuing boxes back to back costs ~180
+    // cycles a box, so four warps share the 16 boxes of a tile.  A K stage
+    // frees as soon as its QK product is done, a V stage after its PV
+    // product; K and V producers run independently.  Block-table entries are
+    // staged in shared memory, kTblWin at a time, with coalesced loads.
+    const int pw = warp - 5;
+    const bool is_v = pw >= 2;
+    const int half = pw & 1;
+    const CUtensorMap* tm = is_v ? &tmV : &tmK;
+    uint64_t* full = is_v ? bars.v_full : bars.k_full;
+    uint64_t* empty = is_v ? bars.v_empty : bars.k_empty;
+    const uint32_t ring = (is_v ? sV : sK) + half * kBox;
+    int* tbl = tbl_sh[pw];
+    int issued = 0, win = -1;
+    bool ok = true;
+    for (int j = 0; j < ntile && ok; ++j) {
+      if (win < 0 || j * kTB + kTB > win + kTblWin) {
+        __syncwarp();
+        win = j * kTB;
+        for (int i = lane; i < kTblWin; i += 32) {
+          const int jb = it.blk_begin + win + i;
+          tbl[i] = jb < it.blk_end ? table[jb] : -1;
         }
-        if (*(volatile int*)&abort_sh) break;
-        const uint32_t fb = smem_u32(&bars.kv_full[s]);
-        mbar_expect_tx(fb, kStage);
-        const uint32_t kst = sKV + s * kStage, vst = kst + kKV;
-        for (int i = 0; i < kTB; ++i) {
-          const int jb = it.blk_begin + j * kTB + i;
-          int64_t y = oob_row;  // zero fill past the range
-          if (jb < it.blk_end) {
-            const int phys = table[jb];
-            if (phys >= 0 && (int64_t)phys < p.num_blocks)
-              y = ((int64_t)phys * p.Hkv + it.g) * 16;
-            else
-              record_status(p.status, KV_ERR_DEVICE, phys);
-          }
-          for (int bx = 0; bx < 2; ++bx) {
-            tma_load_2d(kst + bx * kBox + i * 2048, &tmK, bx * 64, (int)y, fb);
-            tma_load_2d(vst + bx * kBox + i * 2048, &tmV, bx * 64, (int)y, fb);
-          }
-        }
-        issued = j + 1;
+        __syncwarp();
       }
-      // Let every load this CTA issued land before it can exit.
-      const int first = issued > kNS ? issued - kNS : 0;
-      for (int j = first; j < issued; ++j)
-        mbar_wait(smem_u32(&bars.kv_full[j % kNS]), (j / kNS) & 1);
+      const int s = j % kNS;
+      if (lane == 0) {
+        if (*(volatile int*)&abort_sh ||
+            (j >= kNS && !mbar_wait(smem_u32(&empty[s]), ((j / kNS) - 1) & 1)))
+          ok = false;
+        else
+          mbar_expect_tx(smem_u32(&full[s]), kBox);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (lane < kTB) {
+        const int rel = j * kTB + lane;
+        int64_t y = oob_row;  // zero fill past the range
+        if (it.blk_begin + rel < it.blk_end) {
+          const int phys = tbl[rel - win];
+          if (phys >= 0 && (int64_t)phys < p.num_blocks)
+            y = ((int64_t)phys * p.Hkv + it.g) * 16;
+          else if (pw == 0)
+            record_status(p.status, KV_ERR_DEVICE, phys);
+        }
+        tma_load_2d(ring + s * kKV + lane * 2048, tm, half * 64, (int)y,
+                    smem_u32(&full[s]));
+      }
+      __syncwarp();
+      issued = j + 1;
     }
-  } else if (warp == 5) {
+    if (lane == 0) {
+      if (!ok && !*(volatile int*)&abort_sh) {
+        record_status(p.status, KV_ERR_TIMEOUT, 10);
+        atomicExch(&abort_sh, 1);
+      }
+      // Let every load this warp issued land before the CTA can exit.
+      for (int j = issued > kNS ? issued - kNS : 0; j < issued; ++j)
+        mbar_wait(smem_u32(&full[j % kNS]), (j / kNS) & 1);
+    }
+  } else if (warp == kMmaWarp) {
     // ---- MMA issuer ------------------------------------------------------
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc(128, kT, false);
@@ -269,26 +302,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto pv = [&](int jp) {
         const int b = jp & 1, s = jp % kNS;
         if (!mbar_wait(smem_u32(&bars.p_full[b]), (jp >> 1) & 1)) return false;
+        if (!mbar_wait(smem_u32(&bars.v_full[s]), (jp / kNS) & 1)) return false;
         fence_after_sync();
-        const uint32_t vst = sKV + s * kStage + kKV;
+        const uint32_t vst = sV + s * kKV;
 #pragma unroll
         for (int kt = 0; kt < kT / 16; ++kt) {
           const uint64_t a = sdesc(sP + b * kPBytes + kt * 32, 16, 1024);
           const uint64_t bd = sdesc(vst + kt * 2048, kBox, 1024);
           umma(tmem + 128, a, bd, id_pv, (jp > 0 || kt > 0) ? 1u : 0u);
         }
-        umma_commit(smem_u32(&bars.kv_empty[s]));
+        umma_commit(smem_u32(&bars.v_empty[s]));
         umma_commit(smem_u32(&bars.pv_done[b]));
         return true;
       };
       for (int j = 0; j < ntile && ok; ++j) {
         const int s = j % kNS, b = j & 1;
-        if (!mbar_wait(smem_u32(&bars.kv_full[s]), (j / kNS) & 1)) {
+        if (!mbar_wait(smem_u32(&bars.k_full[s]), (j / kNS) & 1)) {
           ok = false;
           break;
         }
         fence_after_sync();
-        const uint32_t kst = sKV + s * kStage;
+        const uint32_t kst = sK + s * kKV;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t a = sdesc(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16,
@@ -297,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     1024);
           umma(tmem + b * kT, a, bd, id_qk, kk > 0 ? 1u : 0u);
         }
+        umma_commit(smem_u32(&bars.k_empty[s]));
         umma_commit(smem_u32(&bars.s_full[b]));
         if (j >= 1) ok = pv(j - 1);
       }
@@ -328,12 +363,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(lane_base + b * kT + 32, sv[1]);
       tmem_wait_ld();
       const int valid = min(kT, (it.blk_end - (it.blk_begin + j * kTB)) * 16);
-      float mx = -INFINITY;
+      if (valid < kT) {
+        // Past the range: -inf, so these tokens weigh exactly 0.
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+        for (int c = 0; c < kT; ++c)
+          if (c >= valid) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+      }
+      float mx8[8];
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (h * 32 + c < valid) mx = fmaxf(mx, __uint_as_float(sv[h][c]));
+      for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(sv[i >> 2][(i & 3) * 8]);
+#pragma unroll
+      for (int c = 0; c < kT; ++c)
+        if ((c & 7) != 0)
+          mx8[c >> 3] = fmaxf(mx8[c >> 3], __uint_as_float(sv[c >> 5][c & 31]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_tile = mx * p.scale_log2;
       const bool need = m_tile > m_used + kRescale;
       const float m_new = need ? m_tile : m_used;
@@ -366,22 +410,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const uint32_t prow = sP + b * kPBytes + r * 128;
+      const float neg_m = -m_used;
+      float l8[8];
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
         uint32_t w4[4];
+        float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int c0 = ch * 8 + 2 * e;
-          const float s0 = __uint_as_float(sv[c0 >> 5][c0 & 31]);
-          const float s1 = __uint_as_float(sv[(c0 + 1) >> 5][(c0 + 1) & 31]);
-          const float p0 = c0 < valid ? ex2(s0 * p.scale_log2 - m_used) : 0.f;
-          const float p1 =
-              c0 + 1 < valid ? ex2(s1 * p.scale_log2 - m_used) : 0.f;
-          l += p0 + p1;
+          const float p0 =
+              ex2(fmaf(__uint_as_float(sv[c0 >> 5][c0 & 31]), p.scale_log2, neg_m));
+          const float p1 = ex2(fmaf(__uint_as_float(sv[(c0 + 1) >> 5][(c0 + 1) & 31]),
+                                    p.scale_log2, neg_m));
+          acc += p0 + p1;
           w4[e] = pack_bf16(p0, p1);
         }
+        l8[ch] = acc;
         st_shared_v4(prow + ((ch ^ (r & 7)) << 4), w4[0], w4[1], w4[2], w4[3]);
       }
+      l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
       fence_proxy_async_smem();
       fence_before_sync();
       __syncwarp();
@@ -418,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     asm volatile(
         "tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
         "r"(kTmemCols)
