@@ -33,15 +33,16 @@ namespace tc {
 
 constexpr int kT = 64;                   // tokens per KV tile
 constexpr int kTB = kT / 16;             // blocks per KV tile
-constexpr int kNS = 4;                   // stages of each of the K and V rings
+constexpr int kNS = 5;                   // stages of each of the K and V rings
 constexpr int kBox = kT * 128;           // one 64-column box of a K/V tile
 constexpr int kKV = 2 * kBox;            // K (or V) tile, head_dim 128
-constexpr int kQBytes = 2 * 128 * 128;   // Q: 2 boxes x 128 rows x 128 B
-constexpr int kPBytes = 128 * kT * 2;    // P: 128 rows x 64 tokens bf16
-constexpr int kSmem = kQBytes + 2 * kPBytes + 2 * kNS * kKV + 1024;
+constexpr int kSmem = 2 * kNS * kKV + 1024;
 constexpr int kThreads = 288;            // warps 0-3 rows, 4 MMA, 5-8 TMA
 constexpr int kMmaWarp = 4;
-constexpr uint32_t kTmemCols = 256;      // S[0] 0..63, S[1] 64..127, O 128..255
+// TMEM columns (fp32 unless noted): S[0] 0..63, S[1] 64..127, P[0] 128..159
+// and P[1] 160..191 (bf16 pairs), O 192..319, Q 320..383 (bf16 pairs).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColP = 128, kColO = 192, kColQ = 320;
 constexpr float kRescale = 8.f;          // lazy-max threshold (log2 units)
 constexpr int kTblWin = 128;             // block-table entries staged at once
 
@@ -71,6 +72,19 @@ __device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b,
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
           tmem_d),
       "l"(a), "l"(b), "r"(id), "r"(accumulate)
+      : "memory");
+}
+
+// Same with A read from tensor memory (16-bit A: two elements per column).
+__device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a,
+                                        uint64_t b, uint32_t id,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+          tmem_d),
+      "r"(tmem_a), "l"(b), "r"(id), "r"(accumulate)
       : "memory");
 }
 
@@ -162,9 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sQ = base;
-  const uint32_t sP = base + kQBytes;              // P[0], P[1]
-  const uint32_t sK = sP + 2 * kPBytes;            // K ring
+  const uint32_t sK = base;                        // K ring
   const uint32_t sV = sK + kNS * kKV;              // V ring
   const WorkItem it = items[blockIdx.x];
   if (!item_ok(it, p, 128)) {
@@ -206,7 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  // Q tile: row r = (branch, q-head) of the segment, 128B-swizzled K-major.
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  // Q tile into TMEM columns kColQ.. (lane r = row r = (branch, q-head) of
+  // the segment; column c holds elements 2c and 2c + 1).
   if (threadIdx.x < 128) {
     const int r = threadIdx.x;
     const uint4* src = nullptr;
@@ -216,15 +232,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qh = it.g * p.G + rr % p.G;
       src = reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.Hq + qh) * 128);
     }
+    const uint32_t lane_base = tmem_base_sh + ((uint32_t)(warp * 32) << 16);
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const uint4 v = src ? src[c] : make_uint4(0, 0, 0, 0);
-      const uint32_t a = sQ + (c >> 3) * 16384 + r * 128 +
-                         (((c & 7) ^ (r & 7)) << 4);
-      st_shared_v4(a, v.x, v.y, v.z, v.w);
+    for (int h = 0; h < 2; ++h) {
+      uint32_t qv[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = src ? src[h * 8 + c] : make_uint4(0, 0, 0, 0);
+        qv[4 * c] = v.x;
+        qv[4 * c + 1] = v.y;
+        qv[4 * c + 2] = v.z;
+        qv[4 * c + 3] = v.w;
+      }
+      tmem_st32(lane_base + kColQ + h * 32, qv);
     }
-    fence_proxy_async_smem();
+    tmem_wait_st();
   }
+  // Q must be in TMEM before the first QK product is issued.
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
@@ -307,9 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vst = sV + s * kKV;
 #pragma unroll
         for (int kt = 0; kt < kT / 16; ++kt) {
-          const uint64_t a = sdesc(sP + b * kPBytes + kt * 32, 16, 1024);
           const uint64_t bd = sdesc(vst + kt * 2048, kBox, 1024);
-          umma(tmem + 128, a, bd, id_pv, (jp > 0 || kt > 0) ? 1u : 0u);
+          umma_ts(tmem + kColO, tmem + kColP + b * (kT / 2) + kt * 8, bd,
+                  id_pv, (jp > 0 || kt > 0) ? 1u : 0u);
         }
         umma_commit(smem_u32(&bars.v_empty[s]));
         umma_commit(smem_u32(&bars.pv_done[b]));
@@ -325,11 +349,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kst = sK + s * kKV;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = sdesc(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16,
-                                   1024);
           const uint64_t bd = sdesc(kst + (kk >> 2) * kBox + (kk & 3) * 32, 16,
                                     1024);
-          umma(tmem + b * kT, a, bd, id_qk, kk > 0 ? 1u : 0u);
+          umma_ts(tmem + b * kT, tmem + kColQ + kk * 8, bd, id_qk,
+                  kk > 0 ? 1u : 0u);
         }
         umma_commit(smem_u32(&bars.k_empty[s]));
         umma_commit(smem_u32(&bars.s_full[b]));
@@ -392,29 +415,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t ov[32];
-          tmem_ld32(lane_base + 128 + c * 32, ov);
+          tmem_ld32(lane_base + kColO + c * 32, ov);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st32(lane_base + 128 + c * 32, ov);
+          tmem_st32(lane_base + kColO + c * 32, ov);
         }
         tmem_wait_st();
       }
       l *= alpha;
       m_used = m_new;
-      // P row (bf16) for this tile.
+      // P[b] is free once PV(j - 2) is done.
       if (j >= 2 &&
           !mbar_wait(smem_u32(&bars.pv_done[b]), ((j - 2) >> 1) & 1)) {
         ok = false;
         break;
       }
-      const uint32_t prow = sP + b * kPBytes + r * 128;
+      // P row (bf16 pairs) into this row's TMEM lane, columns P[b].
       const float neg_m = -m_used;
+      uint32_t pk[kT / 2];
       float l8[8];
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
-        uint32_t w4[4];
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -424,13 +447,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float p1 = ex2(fmaf(__uint_as_float(sv[(c0 + 1) >> 5][(c0 + 1) & 31]),
                                     p.scale_log2, neg_m));
           acc += p0 + p1;
-          w4[e] = pack_bf16(p0, p1);
+          pk[c0 >> 1] = pack_bf16(p0, p1);
         }
         l8[ch] = acc;
-        st_shared_v4(prow + ((ch ^ (r & 7)) << 4), w4[0], w4[1], w4[2], w4[3]);
       }
       l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-      fence_proxy_async_smem();
+      tmem_st32(lane_base + kColP + b * (kT / 2), pk);
+      tmem_wait_st();
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[b]));
@@ -449,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t ov[32];
-        tmem_ld32(lane_base + 128 + c * 32, ov);
+        tmem_ld32(lane_base + kColO + c * 32, ov);
         tmem_wait_ld();
         if (r < it.nrows) {
 #pragma unroll
