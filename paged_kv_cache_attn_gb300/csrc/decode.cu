@@ -356,35 +356,33 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const MergeParams p) {
   const int b = gw / p.Hq, h = gw % p.Hq;
   const int g = h / p.G, r = h % p.G;
   const int e0 = p.csr_ptr[b], e1 = p.csr_ptr[b + 1];
-  float mstar = -INFINITY;
-  for (int e = e0; e < e1; ++e) {
-    const MergeEntry me = p.csr[e];
-    if (r < me.r_lo || r >= me.r_hi) continue;
-    const int64_t row = me.base + (int64_t)g * me.stride + (r - me.r_lo);
-    if (row < 0 || row >= p.partial_rows) continue;
-    mstar = fmaxf(mstar, p.ml[row].x);
-  }
-  const float muse = mstar == -INFINITY ? 0.f : mstar;
+  // One pass with a running maximum: m (base-2 log units), l, acc.
+  float m = -INFINITY, lsum = 0.f;
   float acc[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.f;
-  float lsum = 0.f;
   for (int e = e0; e < e1; ++e) {
     const MergeEntry me = p.csr[e];
     if (r < me.r_lo || r >= me.r_hi) continue;
     const int64_t row = me.base + (int64_t)g * me.stride + (r - me.r_lo);
     if (row < 0 || row >= p.partial_rows) continue;
     const float2 ml = p.ml[row];
-    const float w = ex2(ml.x - muse);
-    lsum += w * ml.y;
     const float* src = p.o + (int64_t)row * D + lane * V;
+    float v[V];
     if constexpr (V == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(src);
-      acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+      const float4 t = *reinterpret_cast<const float4*>(src);
+      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
     } else {
-      const float2 v = *reinterpret_cast<const float2*>(src);
-      acc[0] += w * v.x; acc[1] += w * v.y;
+      const float2 t = *reinterpret_cast<const float2*>(src);
+      v[0] = t.x; v[1] = t.y;
     }
+    const float m_new = fmaxf(m, ml.x);
+    const float a = m == -INFINITY ? 0.f : ex2(m - m_new);  // first entry: 0
+    const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - m_new);
+    lsum = lsum * a + w * ml.y;
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = acc[i] * a + w * v[i];
+    m = m_new;
   }
   const float inv = 1.f / lsum;
   __nv_bfloat16* dst = p.out + ((int64_t)b * p.Hq + h) * D + lane * V;
@@ -468,6 +466,38 @@ cudaError_t launch_merge(const MergeParams& mp, cudaStream_t stream) {
 cudaError_t launch_tile_items(const CUtensorMap& tk, const CUtensorMap& tv,
                               const SplitParams& sp, const WorkItem* items,
                               int n_items, int d, cudaStream_t stream);
+
+// Second stream (and fork / join events) per device: the tensor-core tile
+// pass runs beside the split-KV pass so that the tile kernel's tensor work
+// overlaps the split kernel's HBM streaming on the same SMs.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+kv_status side_stream(SideStream** out) {
+  static std::mutex mu;
+  static SideStream per_dev[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64)
+    return fail(KV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  std::lock_guard<std::mutex> lock(mu);
+  SideStream& s = per_dev[dev];
+  if (!s.stream) {
+    e = cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess)
+      e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess)
+      e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      s.stream = nullptr;
+      return fail(KV_ERR_CUDA, "side stream: %s", cudaGetErrorString(e));
+    }
+  }
+  *out = &s;
+  return KV_OK;
+}
 
 thread_local void* const* g_launch_events = nullptr;
 thread_local int g_n_launch_events = 0;
@@ -555,14 +585,31 @@ extern "C" kv_status paged_decode_attn(
 
   cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(pkv::DeviceStatus), st);
   if (e != cudaSuccess) return fail(KV_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+  // With both passes present the tile pass forks onto the side stream and
+  // joins back before the merge.
+  pkv::SideStream* side = nullptr;
+  const bool fork = info->n_tile_items > 0 && info->n_row_items > 0;
+  if (fork) {
+    if (kv_status s2 = pkv::side_stream(&side)) return s2;
+    e = cudaEventRecord(side->fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+    if (e != cudaSuccess)
+      return fail(KV_ERR_CUDA, "fork: %s", cudaGetErrorString(e));
+  }
   if (info->n_tile_items > 0) {
-    pkv::mark(0, st);
+    cudaStream_t ts = fork ? side->stream : st;
+    pkv::mark(0, ts);
     e = pkv::launch_tile_items(
         tk, tv, sp, reinterpret_cast<const pkv::WorkItem*>(plan + off_tile),
-        info->n_tile_items, d, st);
-    pkv::mark(1, st);
+        info->n_tile_items, d, ts);
+    pkv::mark(1, ts);
     if (e != cudaSuccess)
       return fail(KV_ERR_CUDA, "tile kernel: %s", cudaGetErrorString(e));
+    if (fork) {
+      e = cudaEventRecord(side->join, ts);
+      if (e != cudaSuccess)
+        return fail(KV_ERR_CUDA, "join: %s", cudaGetErrorString(e));
+    }
   }
   if (info->n_row_items > 0) {
     sp.items = reinterpret_cast<const pkv::WorkItem*>(plan + off_row);
@@ -572,6 +619,11 @@ extern "C" kv_status paged_decode_attn(
     pkv::mark(3, st);
     if (e != cudaSuccess)
       return fail(KV_ERR_CUDA, "split-KV kernel: %s", cudaGetErrorString(e));
+  }
+  if (fork) {
+    e = cudaStreamWaitEvent(st, side->join, 0);
+    if (e != cudaSuccess)
+      return fail(KV_ERR_CUDA, "join: %s", cudaGetErrorString(e));
   }
   pkv::MergeParams mp;
   mp.csr_ptr = plan + off_ptr;

@@ -8,18 +8,21 @@
 // RKSC summary §1.1 on cross-branch KV waste) -- and the contraction is dense
 // enough (up to 128 flops per KV byte) to belong on the tensor cores.
 //
-// Pipeline per 64-token KV tile j (4 blocks of 16):
-//   warps 5-8 (TMA):   K and V, each as two column halves: 4 boxes (16 rows
-//                      x 64 cols, 128-byte swizzle) per warp and tile into
-//                      stage j % 4 -> k_full / v_full
-//   warp 4  (MMA):     S[j%2] = Q K^T  (M=128, N=64, K=128; TMEM, fp32)
-//                      -> s_full, k_empty; then O += P(j-1) V(j-1) (M=128,
-//                      N=128, K=64; V as an MN-major operand) -> v_empty,
-//                      pv_done
-//   warps 0-3 (rows):  thread r owns row r: S row from TMEM, base-2 online
-//                      softmax with a lazy maximum (O and l are rescaled only
-//                      when the row maximum grows by more than 8, so p <= 256),
-//                      P row (bf16) into 128B-swizzled shared memory -> p_full
+// Pipeline per 128-token KV tile j (8 blocks of 16):
+//   warps 5-8 (TMA):   K and V, each as two column halves: 8 boxes (16 rows
+//                      x 64 cols, 128-byte swizzle) per warp and tile, one
+//                      per lane, into stage j % 2 -> k_full / v_full
+//   warp 4  (MMA):     S[j%2] = Q K^T  (M=128, N=128, K=128; Q and S in
+//                      TMEM) -> s_full, k_empty; then O += P(j-1) V(j-1)
+//                      (M=128, N=128, K=128; P in TMEM, V as an MN-major
+//                      shared-memory operand) -> v_empty, pv_done
+//   warps 0-3 (rows):  thread r owns row r: two passes over its S row in
+//                      TMEM (maximum, then P = 2^(s - m) as bf16 pairs into
+//                      TMEM), base-2 online softmax with a lazy maximum (O and
+//                      l are rescaled only when the row maximum grows by more
+//                      than 8, so p <= 256) -> p_full
+// An MMA of M=128, K=16 costs about the same ~95 cycles for N=64 and N=128
+// on this part, so 128-token tiles halve the QK cost per token.
 // At the end the rows read O from TMEM and write unnormalised partials
 // (o, m, l), merged with the other passes by log-sum-exp.
 //
@@ -31,18 +34,18 @@
 namespace pkv {
 namespace tc {
 
-constexpr int kT = 64;                   // tokens per KV tile
+constexpr int kT = 128;                  // tokens per KV tile
 constexpr int kTB = kT / 16;             // blocks per KV tile
-constexpr int kNS = 5;                   // stages of each of the K and V rings
+constexpr int kNS = 2;                   // stages of each of the K and V rings
 constexpr int kBox = kT * 128;           // one 64-column box of a K/V tile
 constexpr int kKV = 2 * kBox;            // K (or V) tile, head_dim 128
 constexpr int kSmem = 2 * kNS * kKV + 1024;
 constexpr int kThreads = 288;            // warps 0-3 rows, 4 MMA, 5-8 TMA
 constexpr int kMmaWarp = 4;
-// TMEM columns (fp32 unless noted): S[0] 0..63, S[1] 64..127, P[0] 128..159
-// and P[1] 160..191 (bf16 pairs), O 192..319, Q 320..383 (bf16 pairs).
+// TMEM columns (fp32 unless noted): S[0] 0..127, S[1] 128..255, P 256..319
+// (bf16 pairs), O 320..447, Q 448..511 (bf16 pairs).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColP = 128, kColO = 192, kColQ = 320;
+constexpr uint32_t kColP = 256, kColO = 320, kColQ = 448;
 constexpr float kRescale = 8.f;          // lazy-max threshold (log2 units)
 constexpr int kTblWin = 128;             // block-table entries staged at once
 
@@ -141,6 +144,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr,
       : "memory");
 }
 
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr,
+                                          const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+      "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]),
+      "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -157,9 +172,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a,
                : "memory");
 }
 
+// Named barrier 1: the four softmax warps and the MMA warp (Q is in TMEM).
+__device__ __forceinline__ void q_ready_barrier() {
+  asm volatile("bar.sync 1, %0;" ::"r"(5 * 32) : "memory");
+}
+
 struct Bars {
   uint64_t k_full[kNS], k_empty[kNS], v_full[kNS], v_empty[kNS], s_full[2],
-      p_full[2], pv_done[2], o_ready, drain;
+      p_full, pv_done, o_ready, drain;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -195,11 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars.v_full[s]), 2);   // two V producer warps
       mbar_init(smem_u32(&bars.v_empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&bars.s_full[b]), 1);
-      mbar_init(smem_u32(&bars.p_full[b]), 4);
-      mbar_init(smem_u32(&bars.pv_done[b]), 1);
-    }
+    for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&bars.s_full[b]), 1);
+    mbar_init(smem_u32(&bars.p_full), 4);
+    mbar_init(smem_u32(&bars.pv_done), 1);
     mbar_init(smem_u32(&bars.o_ready), 1);
     mbar_init(smem_u32(&bars.drain), 1);
     abort_sh = 0;
@@ -248,10 +266,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tmem_wait_st();
   }
-  // Q must be in TMEM before the first QK product is issued.
-  fence_before_sync();
-  __syncthreads();
-  fence_after_sync();
+  // Q must be in TMEM before the first QK product is issued; the producer
+  // warps do not wait for it and start loading K and V at once.
+  if (warp <= kMmaWarp) {
+    fence_before_sync();
+    q_ready_barrier();
+    fence_after_sync();
+  }
   const uint32_t tmem = tmem_base_sh;
 
   if (warp >= 5) {
@@ -324,19 +345,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_pv = idesc(128, 128, true);
       bool ok = true;
       auto pv = [&](int jp) {
-        const int b = jp & 1, s = jp % kNS;
-        if (!mbar_wait(smem_u32(&bars.p_full[b]), (jp >> 1) & 1)) return false;
+        const int s = jp % kNS;
+        if (!mbar_wait(smem_u32(&bars.p_full), jp & 1)) return false;
         if (!mbar_wait(smem_u32(&bars.v_full[s]), (jp / kNS) & 1)) return false;
         fence_after_sync();
         const uint32_t vst = sV + s * kKV;
 #pragma unroll
         for (int kt = 0; kt < kT / 16; ++kt) {
           const uint64_t bd = sdesc(vst + kt * 2048, kBox, 1024);
-          umma_ts(tmem + kColO, tmem + kColP + b * (kT / 2) + kt * 8, bd,
-                  id_pv, (jp > 0 || kt > 0) ? 1u : 0u);
+          umma_ts(tmem + kColO, tmem + kColP + kt * 8, bd, id_pv,
+                  (jp > 0 || kt > 0) ? 1u : 0u);
         }
         umma_commit(smem_u32(&bars.v_empty[s]));
-        umma_commit(smem_u32(&bars.pv_done[b]));
+        umma_commit(smem_u32(&bars.pv_done));
         return true;
       };
       for (int j = 0; j < ntile && ok; ++j) {
@@ -381,37 +402,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       fence_after_sync();
-      uint32_t sv[2][32];
-      tmem_ld32(lane_base + b * kT, sv[0]);
-      tmem_ld32(lane_base + b * kT + 32, sv[1]);
-      tmem_wait_ld();
+      const uint32_t srow = lane_base + b * kT;
       const int valid = min(kT, (it.blk_end - (it.blk_begin + j * kTB)) * 16);
-      if (valid < kT) {
-        // Past the range: -inf, so these tokens weigh exactly 0.
+      // Pass 1: row maximum over the tile's valid tokens.
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+      for (int c = 0; c < kT / 32; ++c) {
+        uint32_t sv[32];
+        tmem_ld32(srow + c * 32, sv);
+        tmem_wait_ld();
+        if (valid >= (c + 1) * 32) {
 #pragma unroll
-        for (int c = 0; c < kT; ++c)
-          if (c >= valid) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+          for (int i = 0; i < 32; ++i)
+            mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sv[i]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i < valid)
+              mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sv[i]));
+        }
       }
-      float mx8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(sv[i >> 2][(i & 3) * 8]);
-#pragma unroll
-      for (int c = 0; c < kT; ++c)
-        if ((c & 7) != 0)
-          mx8[c >> 3] = fmaxf(mx8[c >> 3], __uint_as_float(sv[c >> 5][c & 31]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float m_tile = mx * p.scale_log2;
       const bool need = m_tile > m_used + kRescale;
       const float m_new = need ? m_tile : m_used;
       const float alpha = need ? ex2(m_used - m_new) : 1.f;
-      if (__any_sync(0xffffffffu, need) && j > 0) {
-        // O holds PV up to tile j-1: wait for it, then rescale this row.
-        if (!mbar_wait(smem_u32(&bars.pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1)) {
-          ok = false;
-          break;
+      l *= alpha;
+      m_used = m_new;
+      // Pass 2: P = 2^(s * scale_log2 - m) as bf16 pairs, kept in registers
+      // while PV(j - 1) may still be reading the P columns.
+      const float neg_m = -m_used;
+      uint32_t pk[kT / 2];
+#pragma unroll
+      for (int c = 0; c < kT / 32; ++c) {
+        uint32_t sv[32];
+        tmem_ld32(srow + c * 32, sv);
+        tmem_wait_ld();
+        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int t0 = c * 32 + 2 * i;
+          float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), p.scale_log2, neg_m));
+          float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), p.scale_log2, neg_m));
+          p0 = t0 < valid ? p0 : 0.f;
+          p1 = t0 + 1 < valid ? p1 : 0.f;
+          acc4[i & 3] += p0 + p1;
+          pk[c * 16 + i] = pack_bf16(p0, p1);
         }
-        fence_after_sync();
+        l += (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+      }
+      // P and O are free of PV(j - 1) once it is done (one P buffer).
+      if (j > 0 && !mbar_wait(smem_u32(&bars.pv_done), (j - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      fence_after_sync();
+      if (__any_sync(0xffffffffu, need) && j > 0) {
+        // Rescale this row of O (it holds PV up to tile j - 1).
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t ov[32];
@@ -422,41 +469,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
           tmem_st32(lane_base + kColO + c * 32, ov);
         }
-        tmem_wait_st();
       }
-      l *= alpha;
-      m_used = m_new;
-      // P[b] is free once PV(j - 2) is done.
-      if (j >= 2 &&
-          !mbar_wait(smem_u32(&bars.pv_done[b]), ((j - 2) >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      // P row (bf16 pairs) into this row's TMEM lane, columns P[b].
-      const float neg_m = -m_used;
-      uint32_t pk[kT / 2];
-      float l8[8];
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        float acc = 0.f;
+      for (int c = 0; c < kT / 32; ++c) {
+        uint32_t q16[16];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c0 = ch * 8 + 2 * e;
-          const float p0 =
-              ex2(fmaf(__uint_as_float(sv[c0 >> 5][c0 & 31]), p.scale_log2, neg_m));
-          const float p1 = ex2(fmaf(__uint_as_float(sv[(c0 + 1) >> 5][(c0 + 1) & 31]),
-                                    p.scale_log2, neg_m));
-          acc += p0 + p1;
-          pk[c0 >> 1] = pack_bf16(p0, p1);
-        }
-        l8[ch] = acc;
+        for (int i = 0; i < 16; ++i) q16[i] = pk[c * 16 + i];
+        tmem_st16(lane_base + kColP + c * 16, q16);
       }
-      l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-      tmem_st32(lane_base + kColP + b * (kT / 2), pk);
       tmem_wait_st();
       fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[b]));
+      if (lane == 0) mbar_arrive(smem_u32(&bars.p_full));
     }
     if (!ok) {
       if (lane == 0) record_status(p.status, KV_ERR_TIMEOUT, 12);

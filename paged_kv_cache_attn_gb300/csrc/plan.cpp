@@ -118,8 +118,11 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
       units.push_back({b, G, shared_end[b], nblk[b], 1, false});
   }
 
-  const int32_t chunk_rows = pick_chunk(units, false, Hkv, num_sms, 64);
-  const int32_t chunk_tile = pick_chunk(units, true, Hkv, num_sms, 128);
+  // Split-KV items: up to 128 blocks.  Tile items: up to 256 blocks (their
+  // 128-row partials are large, so fewer, longer items pay).  Each is halved
+  // while there are fewer than two items per SM.
+  const int32_t chunk_rows = pick_chunk(units, false, Hkv, num_sms, 128);
+  const int32_t chunk_tile = pick_chunk(units, true, Hkv, num_sms, 256);
 
   std::vector<pkv::WorkItem> row_items, tile_items;
   std::vector<std::vector<pkv::MergeEntry>> merge(nb);
