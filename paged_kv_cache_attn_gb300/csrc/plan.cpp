@@ -124,8 +124,15 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   const int32_t chunk_rows = pick_chunk(units, false, Hkv, num_sms, 128);
   const int32_t chunk_tile = pick_chunk(units, true, Hkv, num_sms, 256);
 
+  // Longest units first: their items come first, so the last wave of each
+  // kernel is made of the short ones.  (Items of one unit have equal length
+  // to within one block.)
+  std::stable_sort(units.begin(), units.end(), [](const Unit& x, const Unit& y) {
+    return (x.blk_end - x.blk_begin) > (y.blk_end - y.blk_begin);
+  });
   std::vector<pkv::WorkItem> row_items, tile_items;
-  std::vector<std::vector<pkv::MergeEntry>> merge(nb);
+  struct Tagged { int32_t branch; pkv::MergeEntry e; };
+  std::vector<Tagged> merge_flat;
   int64_t prow = 0;
   for (const Unit& u : units) {
     const int rows_per = u.tile ? pkv::kTileRows : pkv::kRowTile;
@@ -152,21 +159,14 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
         for (int32_t pb = row0 / G; pb * G < row1; ++pb) {
           const int32_t a = std::max(row0, pb * G);
           const int32_t e = std::min(row1, pb * G + G);
-          merge[u.branch0 + pb].push_back(
-              {(int32_t)(base0 + (a - row0)), nrows, a - pb * G, e - pb * G});
+          merge_flat.push_back(
+              {u.branch0 + pb,
+               {(int32_t)(base0 + (a - row0)), nrows, a - pb * G, e - pb * G}});
         }
       }
     }
   }
-  // Longest items first: the last wave is made of the short ones.
-  auto by_len = [](const pkv::WorkItem& x, const pkv::WorkItem& y) {
-    return (x.blk_end - x.blk_begin) > (y.blk_end - y.blk_begin);
-  };
-  std::stable_sort(row_items.begin(), row_items.end(), by_len);
-  std::stable_sort(tile_items.begin(), tile_items.end(), by_len);
-
-  int64_t n_csr = 0;
-  for (auto& m : merge) n_csr += (int64_t)m.size();
+  const int64_t n_csr = (int64_t)merge_flat.size();
   const int64_t off_row = pkv::kPlanHeaderInts;
   const int64_t off_tile = off_row + 8 * (int64_t)row_items.size();
   const int64_t off_ptr = off_tile + 8 * (int64_t)tile_items.size();
@@ -205,20 +205,20 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   h[pkv::H_TOTAL] = (int32_t)total;
   std::memcpy(h + off_row, row_items.data(), row_items.size() * 32);
   std::memcpy(h + off_tile, tile_items.data(), tile_items.size() * 32);
+  // CSR by branch (counting sort, stable).
   int32_t* ptr = h + off_ptr;
   int32_t* ent = h + off_ent;
-  int64_t k = 0;
-  for (int32_t b = 0; b < nb; ++b) {
-    ptr[b] = (int32_t)k;
-    for (auto& e : merge[b]) {
-      ent[4 * k + 0] = e.base;
-      ent[4 * k + 1] = e.stride;
-      ent[4 * k + 2] = e.r_lo;
-      ent[4 * k + 3] = e.r_hi;
-      ++k;
-    }
+  std::fill(ptr, ptr + nb + 1, 0);
+  for (const Tagged& t : merge_flat) ++ptr[t.branch + 1];
+  for (int32_t b = 0; b < nb; ++b) ptr[b + 1] += ptr[b];
+  std::vector<int32_t> fill(ptr, ptr + nb);
+  for (const Tagged& t : merge_flat) {
+    const int32_t k = fill[t.branch]++;
+    ent[4 * k + 0] = t.e.base;
+    ent[4 * k + 1] = t.e.stride;
+    ent[4 * k + 2] = t.e.r_lo;
+    ent[4 * k + 3] = t.e.r_hi;
   }
-  ptr[nb] = (int32_t)k;
   return KV_OK;
 }
 

@@ -510,9 +510,14 @@ extern "C" kv_status kv_build_batch(kv_pool* p, int32_t nb, const int32_t* ids,
   for (int32_t i = 0; i + 1 < nb; ++i) {
     const Node* a = rows[i];
     const Node* c = rows[i + 1];
-    int32_t lim = std::min(a->seq_len / B, c->seq_len / B);
+    const int32_t lim = std::min(a->seq_len / B, c->seq_len / B);
+    const int32_t* x = a->table.data();
+    const int32_t* y = c->table.data();
     int32_t j = 0;
-    while (j < lim && a->table[j] == c->table[j]) ++j;
+    // Whole 64-entry chunks with memcmp, then entry by entry.
+    while (j + 64 <= lim && std::memcmp(x + j, y + j, 64 * sizeof(int32_t)) == 0)
+      j += 64;
+    while (j < lim && x[j] == y[j]) ++j;
     lcp[i] = j;
   }
   std::vector<int32_t> seg;
