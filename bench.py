@@ -109,10 +109,14 @@ def unique_kv_bytes(tables, seq_lens, Hkv, d):
 
 def item_bytes(plan, info, Hkv, d, seq_lens, which):
     """Algorithmic KV bytes one launch of a kernel reads: for each of its work
-    items, the valid tokens of its block range x 2 (K, V) x d x 2 bytes."""
+    items, the valid tokens of its block range x 2 (K, V) x d x 2 bytes.  The
+    two CTAs of a tile-kernel cluster share one read of their common range
+    (TMA multicast), so a pair counts once."""
     off = 16 if which == "row" else 16 + 8 * info.n_row_items
     n = info.n_row_items if which == "row" else info.n_tile_items
     items = plan[off:off + 8 * n].reshape(-1, 8)
+    if which == "tile" and info.tile_cluster > 1:
+        items = items[::info.tile_cluster]
     tot = 0
     for b0, g, row0, nr, lo, hi, pb, masked in items:
         toks = (hi - lo) * 16
@@ -391,6 +395,49 @@ def run_ours(args):
         d2h = pin["out"].numel() * 2
     e2e_s = statistics.median(e2e_t)
 
+    # The same step with every branch re-reading its whole table (no
+    # shared-prefix segments): time and bytes requested, for the sharing
+    # criterion (prefix bytes moved shared vs per-branch re-read).
+    sharing = None
+    if len(bt.groups):
+        bu = cache.batch(flags=B.KV_PLAN_IGNORE_GROUPS).upload()
+        for _ in range(3):
+            bu.decode(q, out)
+        n_u = 20
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n_u):
+            bu.decode(q, out)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_u = e0.elapsed_time(e1) / n_u
+        bytes_shared = sum(item_bytes(bt.plan, bt.info, w.Hkv, w.d,
+                                      bt.seq_lens, k) for k in ("row", "tile"))
+        bytes_unshared = item_bytes(bu.plan, bu.info, w.Hkv, w.d, bu.seq_lens,
+                                    "row")
+        kvb = 2 * w.d * 2 * w.Hkv * 16  # bytes per block, all kv-heads
+        pref_unshared = int(sum(int(g[1]) * int(g[3]) for g in bt.groups)) * kvb
+        pref_shared = 0
+        for g in bt.groups:
+            rows = int(g[1]) * (w.Hq // w.Hkv)
+            if rows >= 65 and w.d == 128:        # tcgen05 tiles, paired
+                loads = -(-rows // (128 * bt.info.tile_cluster))
+            else:                                 # 16-row split items
+                loads = -(-rows // 16)
+            pref_shared += loads * int(g[3]) * kvb
+        sharing = {
+            "ms_per_step_shared": round(ms_step, 5),
+            "ms_per_step_per_branch_reread": round(ms_u, 5),
+            "speedup": round(ms_u / ms_step, 3),
+            "bytes_requested_shared": bytes_shared,
+            "bytes_requested_per_branch_reread": bytes_unshared,
+            "prefix_bytes_shared": pref_shared,
+            "prefix_bytes_per_branch_reread": pref_unshared,
+            "prefix_bytes_factor": round(pref_unshared / max(pref_shared, 1), 2),
+        }
+
     res = None
     if rank == 0:
         clocks = clk.summary()
@@ -446,6 +493,7 @@ def run_ours(args):
                 "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
             },
+            "sharing": sharing,
             "gpu_launches": launches_per_step * K,
             "clocks": clocks,
         }

@@ -220,6 +220,10 @@ typedef struct kv_decode_plan_info {
   int32_t n_tile_items;    /* 128-row work items of the tcgen05 kernel */
   int32_t n_merge_rows;    /* nb (one merge per branch and kv-head) */
   int32_t chunk_blocks;    /* blocks per split-KV item */
+  int32_t tile_cluster;    /* CTAs per cluster of the tcgen05 kernel (1 or 2):
+                              with 2, the two 128-row tiles of one segment
+                              share every K/V load (TMA multicast) */
+  int32_t reserved;
 } kv_decode_plan_info;
 
 /* Host half of a decode step: split the step into work items.

@@ -465,7 +465,8 @@ cudaError_t launch_merge(const MergeParams& mp, cudaStream_t stream) {
 // Tensor-core (tcgen05) kernel for 128-row tiles; defined in decode_tc.cu.
 cudaError_t launch_tile_items(const CUtensorMap& tk, const CUtensorMap& tv,
                               const SplitParams& sp, const WorkItem* items,
-                              int n_items, int d, cudaStream_t stream);
+                              int n_items, int d, int cluster,
+                              cudaStream_t stream);
 
 // Second stream (and fork / join events) per device: the tensor-core tile
 // pass runs beside the split-KV pass so that the tile kernel's tensor work
@@ -601,7 +602,7 @@ extern "C" kv_status paged_decode_attn(
     pkv::mark(0, ts);
     e = pkv::launch_tile_items(
         tk, tv, sp, reinterpret_cast<const pkv::WorkItem*>(plan + off_tile),
-        info->n_tile_items, d, ts);
+        info->n_tile_items, d, info->tile_cluster, ts);
     pkv::mark(1, ts);
     if (e != cudaSuccess)
       return fail(KV_ERR_CUDA, "tile kernel: %s", cudaGetErrorString(e));

@@ -91,6 +91,40 @@ __device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a,
       : "memory");
 }
 
+// Arrive on the mbarrier at this offset in every CTA of `mask` once this
+// thread's earlier MMAs are done.
+__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster."
+      "multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+// 2-D TMA load written to the same offset in every CTA of `mask`, completing
+// on the mbarrier at `bar` in each of them.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* tm,
+                                               int x, int y, uint32_t bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::"
+      "bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(tm), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
@@ -186,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tile_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
                        const SplitParams p, const WorkItem* items,
-                       int64_t oob_row) {
+                       int64_t oob_row, int cluster) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) Bars bars;
   __shared__ uint32_t tmem_base_sh;
@@ -198,22 +232,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sK = base;                        // K ring
   const uint32_t sV = sK + kNS * kKV;              // V ring
-  const WorkItem it = items[blockIdx.x];
-  if (!item_ok(it, p, 128)) {
+  WorkItem it = items[blockIdx.x];
+  // In a cluster the partner of an odd last tile has no rows (nrows == 0).
+  // A malformed item is recorded and runs with no rows and no tiles; it
+  // still takes part in the cluster barriers so that its partner can finish.
+  const bool good =
+      (it.nrows == 0 && cluster > 1 && it.row0 >= 0 && it.g >= 0 &&
+       it.g < p.Hkv && it.branch0 >= 0 && it.branch0 < p.nb &&
+       it.blk_begin >= 0 && it.blk_begin < it.blk_end &&
+       it.blk_end <= p.max_blocks) ||
+      item_ok(it, p, 128);
+  if (!good) {
     if (threadIdx.x == 0)
       record_status(p.status, KV_ERR_DEVICE, -1 - (int)blockIdx.x);
-    return;
+    it.nrows = 0;
+    it.blk_begin = it.blk_end = 0;
+    it.branch0 = 0;
   }
   const int nblk = it.blk_end - it.blk_begin;
   const int ntile = (nblk + kTB - 1) / kTB;
+  const uint32_t crank = cluster > 1 ? cluster_rank() : 0;
+  const uint16_t cmask = (uint16_t)((1u << cluster) - 1u);
   const int32_t* table = p.tables + (int64_t)it.branch0 * p.max_blocks;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNS; ++s) {
       mbar_init(smem_u32(&bars.k_full[s]), 2);   // two K producer warps
-      mbar_init(smem_u32(&bars.k_empty[s]), 1);
+      mbar_init(smem_u32(&bars.k_empty[s]), cluster);  // every CTA's MMA
       mbar_init(smem_u32(&bars.v_full[s]), 2);   // two V producer warps
-      mbar_init(smem_u32(&bars.v_empty[s]), 1);
+      mbar_init(smem_u32(&bars.v_empty[s]), cluster);
     }
     for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&bars.s_full[b]), 1);
     mbar_init(smem_u32(&bars.p_full), 4);
@@ -237,7 +284,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmV);
   }
   fence_before_sync();
-  __syncthreads();
+  // The partner's barriers must be initialised before any multicast load or
+  // remote arrive reaches them.
+  if (cluster > 1)
+    cluster_sync();
+  else
+    __syncthreads();
   fence_after_sync();
   // Q tile into TMEM columns kColQ.. (lane r = row r = (branch, q-head) of
   // the segment; column c holds elements 2c and 2c + 1).
@@ -313,8 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      if (lane < kTB) {
-        const int rel = j * kTB + lane;
+      if (lane < kTB / cluster) {
+        const int rel = j * kTB + lane * cluster + (int)crank;
         int64_t y = oob_row;  // zero fill past the range
         if (it.blk_begin + rel < it.blk_end) {
           const int phys = tbl[rel - win];
@@ -323,8 +375,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           else if (pw == 0)
             record_status(p.status, KV_ERR_DEVICE, phys);
         }
-        tma_load_2d(ring + s * kKV + lane * 2048, tm, half * 64, (int)y,
-                    smem_u32(&full[s]));
+        const uint32_t dst = ring + s * kKV + (rel - j * kTB) * 2048;
+        if (cluster > 1)
+          tma_load_2d_mc(dst, tm, half * 64, (int)y, smem_u32(&full[s]), cmask);
+        else
+          tma_load_2d(dst, tm, half * 64, (int)y, smem_u32(&full[s]));
       }
       __syncwarp();
       issued = j + 1;
@@ -356,7 +411,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ts(tmem + kColO, tmem + kColP + kt * 8, bd, id_pv,
                   (jp > 0 || kt > 0) ? 1u : 0u);
         }
-        umma_commit(smem_u32(&bars.v_empty[s]));
+        if (cluster > 1)
+          umma_commit_mc(smem_u32(&bars.v_empty[s]), cmask);
+        else
+          umma_commit(smem_u32(&bars.v_empty[s]));
         umma_commit(smem_u32(&bars.pv_done));
         return true;
       };
@@ -375,7 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ts(tmem + b * kT, tmem + kColQ + kk * 8, bd, id_qk,
                   kk > 0 ? 1u : 0u);
         }
-        umma_commit(smem_u32(&bars.k_empty[s]));
+        if (cluster > 1)
+          umma_commit_mc(smem_u32(&bars.k_empty[s]), cmask);
+        else
+          umma_commit(smem_u32(&bars.k_empty[s]));
         umma_commit(smem_u32(&bars.s_full[b]));
         if (j >= 1) ok = pv(j - 1);
       }
@@ -519,13 +580,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         "r"(kTmemCols)
         : "memory");
   }
+  // No CTA leaves while its partner may still write into its shared memory
+  // or arrive on its barriers.
+  if (cluster > 1) cluster_sync();
 }
 
 }  // namespace tc
 
 cudaError_t launch_tile_items(const CUtensorMap& tk, const CUtensorMap& tv,
                               const SplitParams& sp, const WorkItem* items,
-                              int n_items, int d, cudaStream_t stream) {
+                              int n_items, int d, int cluster,
+                              cudaStream_t stream) {
   if (d != 128) return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
@@ -537,9 +602,22 @@ cudaError_t launch_tile_items(const CUtensorMap& tk, const CUtensorMap& tv,
   }
   // A row past the end of the pool's 2-D view: TMA fills the box with zeros.
   const int64_t oob_row = sp.num_blocks * sp.Hkv * 16;
-  tc::tile_decode_kernel<<<n_items, tc::kThreads, tc::kSmem, stream>>>(
-      tk, tv, sp, items, oob_row);
-  return cudaGetLastError();
+  if (cluster < 1 || cluster > 2 || n_items % cluster != 0)
+    return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_items);
+  cfg.blockDim = dim3(tc::kThreads);
+  cfg.dynamicSmemBytes = tc::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc::tile_decode_kernel, tk, tv, sp, items,
+                            oob_row, cluster);
 }
 
 }  // namespace pkv

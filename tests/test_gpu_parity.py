@@ -55,6 +55,9 @@ SMALL = {
     "long_context": lambda: W.long_context(n_indep=3, indep_tokens=1000,
                                            n_roots=2, root_tokens=2048,
                                            fan=16, suffix_tokens=37),
+    "fanout_3tiles": lambda: W.fanout(n_roots=1, root_tokens=512, fan=40,
+                                      min_suffix=1, max_suffix=50, Hq=64,
+                                      Hkv=8),
     "gqa_2": lambda: W.independent(n_seqs=3, min_len=17, max_len=300, Hq=8,
                                    Hkv=4, d=64),
     "gqa_16": lambda: W.fanout(n_roots=1, root_tokens=64, fan=3,

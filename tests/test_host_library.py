@@ -264,6 +264,8 @@ def test_plan_covers_every_token_once(name, flags):
     for it in np.concatenate([rows, tiles]):
         b0, g, row0, nr, lo, hi, pbase, masked = [int(x) for x in it]
         assert 0 <= lo < hi <= nblk[b0]
+        if nr == 0:          # row-less partner of a cluster pair
+            continue
         written[pbase:pbase + nr] += 1
         for r in range(row0, row0 + nr):
             b, qr = b0 + r // G, r % G
@@ -280,7 +282,7 @@ def test_plan_covers_every_token_once(name, flags):
     row_owner = {}
     for it in np.concatenate([rows, tiles]):
         b0, g, row0, nr, lo, hi, pbase, masked = [int(x) for x in it]
-        for r in range(nr):
+        for r in range(nr):  # (row-less partners own no rows)
             row_owner[pbase + r] = (b0 + (row0 + r) // G, g, (row0 + r) % G,
                                     hi - lo)
     for b in range(nb):
@@ -295,6 +297,20 @@ def test_plan_covers_every_token_once(name, flags):
             assert total == nblk[b]
     if flags & B.KV_PLAN_IGNORE_GROUPS:
         assert (rows[:, 7] == 1).all()
+
+
+def test_multi_tile_segments_run_as_pairs():
+    # 40 branches x 8 q-heads = 320 rows: three 128-row tiles, paired with a
+    # row-less partner for the third; both CTAs of a pair read the same blocks.
+    w = W.fanout(n_roots=1, root_tokens=512, fan=40, min_suffix=1,
+                 max_suffix=50, Hq=64, Hkv=8)
+    bt = H.Cache(w, with_data=False).batch(num_sms=152)
+    assert bt.info.tile_cluster == 2 and bt.info.n_tile_items % 2 == 0
+    rows, tiles, ptr, ent = decode_plan(bt.plan, bt.info, bt.nb, w.Hq, w.Hkv)
+    for a, b in zip(tiles[0::2], tiles[1::2]):
+        assert a[0] == b[0] and a[1] == b[1] and (a[4], a[5]) == (b[4], b[5])
+        assert b[2] == a[2] + 128
+    assert (tiles[:, 3] == 0).sum() == 8 * len({(t[4], t[5]) for t in tiles})
 
 
 def test_plan_rejects_bad_input():
