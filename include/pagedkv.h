@@ -259,7 +259,8 @@ kv_status paged_decode_attn_workspace_size(const kv_decode_plan_info* info,
  * 256-byte aligned, no initial contents needed.  Shared-prefix blocks are read
  * once per segment (tensor cores for segments of >= 65 rows).  When a step has
  * both tensor-core tiles and split-KV items, the tile pass runs on a
- * library-owned second stream forked from and joined back into `stream`
+ * library-owned second stream (highest priority) forked from and joined back
+ * into `stream`
  * (event record / wait), so that the two passes overlap; all work is still
  * ordered after earlier work on `stream` and before later work on it.
  * Error behaviour: argument errors return INVALID_ARG before any launch; a

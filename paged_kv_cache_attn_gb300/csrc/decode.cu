@@ -486,7 +486,11 @@ kv_status side_stream(SideStream** out) {
   std::lock_guard<std::mutex> lock(mu);
   SideStream& s = per_dev[dev];
   if (!s.stream) {
-    e = cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking);
+    // Highest priority: the tile pass has fewer, longer CTAs and sits on the
+    // step's critical path, so its pending CTAs are dispatched first.
+    int lo = 0, hi = 0;
+    cudaDeviceGetStreamPriorityRange(&lo, &hi);
+    e = cudaStreamCreateWithPriority(&s.stream, cudaStreamNonBlocking, hi);
     if (e == cudaSuccess)
       e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
     if (e == cudaSuccess)
