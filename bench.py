@@ -58,6 +58,7 @@ def parse():
     ap.add_argument("--workload", default="long_context")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--fused-steps", type=int, default=30)
     return ap.parse_args()
 
 
@@ -438,6 +439,57 @@ def run_ours(args):
             "prefix_bytes_factor": round(pref_unshared / max(pref_shared, 1), 2),
         }
 
+    # NEXT-1: each branch's newest token appended and attended to in one
+    # launch vs a batched one-token append followed by the plain step.  Every
+    # step adds one token per branch (a real decode loop); device time only.
+    fused = None
+    if args.fused_steps > 0:
+        rng = np.random.default_rng(17)
+        kst = torch.from_numpy(W.f32_to_bf16_bits(rng.standard_normal(
+            (nb, w.Hkv, w.d), dtype=np.float32)).view(np.int16)).to(dev) \
+            .view(torch.bfloat16)
+        vst = kst.flip(0).contiguous()
+        ids = cache.decode_ids
+        ones = [1] * nb
+
+        def ev():
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(stream)
+            return e
+
+        # Each step needs up to one new block per branch every 16 tokens;
+        # keep to what the pool's free blocks allow.
+        free = len(B.kv_get_free_stack(cache.h))
+        n_fused = max(1, min(args.fused_steps, 16 * free // (2 * nb) - 4))
+        t_fused, t_unfused = [], []
+        for i in range(n_fused + 2):
+            B.kv_reserve(cache.h, ids, ones)
+            bf = cache.batch().upload()
+            e0 = ev()
+            bf.decode_append(q, kst, vst, out)
+            e1 = ev()
+            torch.cuda.synchronize()
+            if i >= 2:
+                t_fused.append(e0.elapsed_time(e1))
+        for i in range(n_fused + 2):
+            e0 = ev()
+            B.kv_append_batch(cache.h, ids, ones, kst, vst)
+            e1 = ev()
+            bu = cache.batch().upload()
+            e2 = ev()
+            bu.decode(q, out)
+            e3 = ev()
+            torch.cuda.synchronize()
+            if i >= 2:
+                t_unfused.append(e0.elapsed_time(e1) + e2.elapsed_time(e3))
+        fused = {
+            "steps": n_fused,
+            "ms_fused_append_decode": round(statistics.median(t_fused), 5),
+            "ms_append_then_decode": round(statistics.median(t_unfused), 5),
+            "note": "device time per step (events around the launches); the "
+                    "batch is rebuilt on the host between steps",
+        }
+
     res = None
     if rank == 0:
         clocks = clk.summary()
@@ -494,6 +546,7 @@ def run_ours(args):
                 "d2h_bytes_per_step": int(d2h),
             },
             "sharing": sharing,
+            "fused_append": fused,
             "gpu_launches": launches_per_step * K,
             "clocks": clocks,
         }

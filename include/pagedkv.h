@@ -119,6 +119,26 @@ kv_status kv_branch_create(kv_pool* pool, int32_t* out_id);
 kv_status kv_append(kv_pool* pool, int32_t id, int32_t n_tokens,
                     const void* k_new, const void* v_new, void* stream);
 
+/* Batched append (tree expansion: one scatter launch for many branches).
+ * Equivalent to kv_append(ids[i], n_tokens[i], ...) for i = 0..n-1 in order
+ * (same blocks, same order), all or nothing over the whole batch.
+ * k_new, v_new: device [num_layers][total][num_kv_heads][head_dim] bf16 with
+ * total = sum(n_tokens); branch i's rows are rows sum(n_tokens[0..i)) + 0 ..
+ * n_tokens[i]-1.  ids, n_tokens: host.  A branch may appear more than once.
+ * Errors: NOT_FOUND, OOM (no change), INVALID_ARG, CUDA. */
+kv_status kv_append_batch(kv_pool* pool, int32_t n, const int32_t* ids,
+                          const int32_t* n_tokens, const void* k_new,
+                          const void* v_new, void* stream);
+
+/* Reserve n_tokens[i] new token slots at the end of branch ids[i] (blocks
+ * allocated exactly as kv_append_batch would, all or nothing) without
+ * writing any data: the caller writes the rows, e.g. the decode step's new
+ * token with paged_decode_append_attn.  Until written, the slots hold
+ * whatever the blocks held.  Errors: NOT_FOUND, OOM (no change),
+ * INVALID_ARG. */
+kv_status kv_reserve(kv_pool* pool, int32_t n, const int32_t* ids,
+                     const int32_t* n_tokens);
+
 /* Fork a live branch ([TRM] §5 fork rules 1-2, §6 fork_node).  The child
  * shares the parent's full blocks (+1 reference each).  If the parent's last
  * block is partial, the child gets a fresh block holding a copy of that whole
@@ -278,6 +298,26 @@ kv_status paged_decode_attn(const void* q, const void* k_pool,
                             float scale, void* out, const int32_t* plan,
                             const kv_decode_plan_info* info, void* workspace,
                             size_t ws_bytes, void* stream);
+
+/* The decode step fused with the append of each branch's newest token
+ * ([TRM] §2.1: step t+1 caches the new key and value, then attends to all
+ * of them).  Same arguments and result as paged_decode_attn, plus
+ * k_step, v_step: device [nb][Hkv][head_dim] bf16, this layer's K and V of
+ * token seq_lens[b] - 1 of each branch b (its slot reserved beforehand with
+ * kv_reserve and included in block_tables / seq_lens).  In the same launch
+ * the kernel writes those rows into their slots of k_pool / v_pool and
+ * attends to them (it does not read the slot back from the pool).  The
+ * newest token's block is owned by its branch alone (a partial last block is
+ * copied at fork), so it is never inside a shared-prefix segment.
+ * Errors: as paged_decode_attn. */
+kv_status paged_decode_append_attn(
+    const void* q, const void* k_step, const void* v_step, const void* k_pool,
+    const void* v_pool, int64_t num_blocks, const int32_t* block_tables,
+    const int32_t* seq_lens, const int32_t* prefix_groups, int32_t n_groups,
+    int32_t nb, int32_t max_blocks, int32_t Hq, int32_t Hkv, int32_t head_dim,
+    int32_t block_size, float scale, void* out, const int32_t* plan,
+    const kv_decode_plan_info* info, void* workspace, size_t ws_bytes,
+    void* stream);
 
 /* paged_decode_attn without a caller workspace.  The pages have no
  * counterpart: this exists for callers that cannot allocate device memory

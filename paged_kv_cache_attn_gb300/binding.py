@@ -79,6 +79,9 @@ _SIGS = {
     "kv_append": (C.c_int32, [_vp, C.c_int32, C.c_int32, _vp, _vp, _vp]),
     "kv_fork_branch": (C.c_int32, [_vp, C.c_int32, _i32p, _vp]),
     "kv_fork_branches": (C.c_int32, [_vp, C.c_int32, C.c_int32, _i32p, _vp]),
+    "kv_append_batch": (C.c_int32, [_vp, C.c_int32, _i32p, _i32p, _vp, _vp,
+                                    _vp]),
+    "kv_reserve": (C.c_int32, [_vp, C.c_int32, _i32p, _i32p]),
     "kv_free": (C.c_int32, [_vp, C.c_int32]),
     "kv_free_subtree": (C.c_int32, [_vp, C.c_int32, _i32p, _i32p]),
     "kv_evict_order": (C.c_int32, [_vp, C.c_int32, _i32p, _f64p, _i32p]),
@@ -107,6 +110,13 @@ _SIGS = {
                                       C.c_int32, C.c_float, _vp, _vp,
                                       C.POINTER(kv_decode_plan_info), _vp,
                                       C.c_size_t, _vp]),
+    "paged_decode_append_attn": (C.c_int32, [_vp, _vp, _vp, _vp, _vp,
+                                             C.c_int64, _vp, _vp, _vp,
+                                             C.c_int32, C.c_int32, C.c_int32,
+                                             C.c_int32, C.c_int32, C.c_int32,
+                                             C.c_int32, C.c_float, _vp, _vp,
+                                             C.POINTER(kv_decode_plan_info),
+                                             _vp, C.c_size_t, _vp]),
     "paged_decode_attn_noalloc": (C.c_int32, [_vp, _vp, _vp, C.c_int64, _vp,
                                               _vp, _vp, C.c_int32, C.c_int32,
                                               C.c_int32, C.c_int32, C.c_int32,
@@ -202,6 +212,20 @@ def kv_branch_create(h) -> int:
 def kv_append(h, bid, n_tokens, k_new=None, v_new=None, stream=None):
     s = _stream(stream) if k_new is not None else None
     _check(_lib.kv_append(h, bid, n_tokens, _ptr(k_new), _ptr(v_new), s))
+
+
+def kv_append_batch(h, ids, n_tokens, k_new=None, v_new=None, stream=None):
+    ids = _i32(ids)
+    n = _i32(n_tokens)
+    s = _stream(stream) if k_new is not None else None
+    _check(_lib.kv_append_batch(h, len(ids), _as_i32p(ids), _as_i32p(n),
+                                _ptr(k_new), _ptr(v_new), s))
+
+
+def kv_reserve(h, ids, n_tokens):
+    ids = _i32(ids)
+    n = _i32(n_tokens)
+    _check(_lib.kv_reserve(h, len(ids), _as_i32p(ids), _as_i32p(n)))
 
 
 def kv_fork_branch(h, parent, stream=None) -> int:
@@ -369,6 +393,19 @@ def paged_decode_attn(q, k_pool, v_pool, num_blocks, block_tables, seq_lens,
         _ptr(seq_lens), _ptr(prefix_groups), n_groups, nb, max_blocks, Hq, Hkv,
         head_dim, block_size, scale, _ptr(out), _ptr(plan), C.byref(info),
         _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def paged_decode_append_attn(q, k_step, v_step, k_pool, v_pool, num_blocks,
+                             block_tables, seq_lens, prefix_groups, n_groups,
+                             nb, max_blocks, Hq, Hkv, head_dim, scale, out,
+                             plan, info, workspace, ws_bytes, stream=None,
+                             block_size=16):
+    _check(_lib.paged_decode_append_attn(
+        _ptr(q), _ptr(k_step), _ptr(v_step), _ptr(k_pool), _ptr(v_pool),
+        num_blocks, _ptr(block_tables), _ptr(seq_lens), _ptr(prefix_groups),
+        n_groups, nb, max_blocks, Hq, Hkv, head_dim, block_size, scale,
+        _ptr(out), _ptr(plan), C.byref(info), _ptr(workspace), ws_bytes,
+        _stream(stream)))
 
 
 def paged_decode_attn_noalloc(q, k_pool, v_pool, num_blocks, block_tables,

@@ -182,6 +182,30 @@ __global__ void __launch_bounds__(128, 2)
       int nv = seq_len - j * 16;
       nv = nv > 16 ? 16 : nv;
       const uint32_t kt = st, vt = st + C::kTileBytes;
+      if (p.k_step && it.masked && nv < 17 && j * 16 + nv == seq_len) {
+        // Fused append: the branch's newest token (slot nv - 1 of its last
+        // block) comes from k_step / v_step; write it into the tile in shared
+        // memory (swizzled) and into the pool.  Lanes 0-15: K, 16-31: V.
+        const int slot = nv - 1;
+        const int c = lane & 15;
+        if (c < D / 8) {
+          const bool is_v = lane >= 16;
+          const int64_t src =
+              ((int64_t)it.branch0 * p.Hkv + it.g) * (D / 8) + c;
+          const uint4 v = is_v ? p.v_step[src] : p.k_step[src];
+          const uint32_t a = (is_v ? vt : kt) + (c >> 3) * 2048 + slot * 128 +
+                             (((c & 7) ^ (slot & 7)) << 4);
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a),
+                       "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                       : "memory");
+          const int phys = table[j];
+          const int64_t dst =
+              (((int64_t)phys * p.Hkv + it.g) * 16 + slot) * (D / 8) + c;
+          (is_v ? p.v_pool : p.k_pool)[dst] = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
       // S = Q K^T for the block's 16 tokens.
       float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
@@ -524,15 +548,14 @@ extern "C" kv_status kv_set_launch_events(void* const* events,
   return KV_OK;
 }
 
-extern "C" kv_status paged_decode_attn(
-    const void* q, const void* k_pool, const void* v_pool, int64_t num_blocks,
-    const int32_t* block_tables, const int32_t* seq_lens,
-    const int32_t* prefix_groups, int32_t n_groups, int32_t nb,
-    int32_t max_blocks, int32_t Hq, int32_t Hkv, int32_t d, int32_t block_size,
-    float scale, void* out, const int32_t* plan,
+static kv_status decode_impl(
+    const void* q, const void* k_step, const void* v_step, const void* k_pool,
+    const void* v_pool, int64_t num_blocks, const int32_t* block_tables,
+    const int32_t* seq_lens, const int32_t* prefix_groups, int32_t n_groups,
+    int32_t nb, int32_t max_blocks, int32_t Hq, int32_t Hkv, int32_t d,
+    int32_t block_size, float scale, void* out, const int32_t* plan,
     const kv_decode_plan_info* info, void* workspace, size_t ws_bytes,
     void* stream) {
-  pkv::clear_error();
   (void)prefix_groups;
   if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out ||
       !plan || !info || !workspace)
@@ -580,6 +603,10 @@ extern "C" kv_status paged_decode_attn(
   sp.max_blocks = max_blocks;
   sp.num_blocks = num_blocks;
   sp.scale_log2 = scale * 1.4426950408889634f;
+  sp.k_step = static_cast<const uint4*>(k_step);
+  sp.v_step = static_cast<const uint4*>(v_step);
+  sp.k_pool = static_cast<uint4*>(const_cast<void*>(k_pool));
+  sp.v_pool = static_cast<uint4*>(const_cast<void*>(v_pool));
 
   // The plan lives on the device; its layout is fixed by the host header
   // fields mirrored in *info.
@@ -646,6 +673,40 @@ extern "C" kv_status paged_decode_attn(
   if (e != cudaSuccess)
     return fail(KV_ERR_CUDA, "merge kernel: %s", cudaGetErrorString(e));
   return KV_OK;
+}
+
+extern "C" kv_status paged_decode_attn(
+    const void* q, const void* k_pool, const void* v_pool, int64_t num_blocks,
+    const int32_t* block_tables, const int32_t* seq_lens,
+    const int32_t* prefix_groups, int32_t n_groups, int32_t nb,
+    int32_t max_blocks, int32_t Hq, int32_t Hkv, int32_t d, int32_t block_size,
+    float scale, void* out, const int32_t* plan,
+    const kv_decode_plan_info* info, void* workspace, size_t ws_bytes,
+    void* stream) {
+  pkv::clear_error();
+  return decode_impl(q, nullptr, nullptr, k_pool, v_pool, num_blocks,
+                     block_tables, seq_lens, prefix_groups, n_groups, nb,
+                     max_blocks, Hq, Hkv, d, block_size, scale, out, plan, info,
+                     workspace, ws_bytes, stream);
+}
+
+extern "C" kv_status paged_decode_append_attn(
+    const void* q, const void* k_step, const void* v_step, const void* k_pool,
+    const void* v_pool, int64_t num_blocks, const int32_t* block_tables,
+    const int32_t* seq_lens, const int32_t* prefix_groups, int32_t n_groups,
+    int32_t nb, int32_t max_blocks, int32_t Hq, int32_t Hkv, int32_t d,
+    int32_t block_size, float scale, void* out, const int32_t* plan,
+    const kv_decode_plan_info* info, void* workspace, size_t ws_bytes,
+    void* stream) {
+  pkv::clear_error();
+  if (!k_step || !v_step)
+    return fail(KV_ERR_INVALID_ARG, "k_step / v_step required");
+  if (((uintptr_t)k_step | (uintptr_t)v_step) & 15)
+    return fail(KV_ERR_INVALID_ARG, "k_step / v_step must be 16-byte aligned");
+  return decode_impl(q, k_step, v_step, k_pool, v_pool, num_blocks,
+                     block_tables, seq_lens, prefix_groups, n_groups, nb,
+                     max_blocks, Hq, Hkv, d, block_size, scale, out, plan, info,
+                     workspace, ws_bytes, stream);
 }
 
 extern "C" kv_status kv_check_device_status(void* workspace, void* stream,

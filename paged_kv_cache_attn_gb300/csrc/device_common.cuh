@@ -142,6 +142,13 @@ struct SplitParams {
   int64_t num_blocks;
   int64_t partial_rows;
   float scale_log2;
+  // Fused append (paged_decode_append_attn): this layer's K/V of each
+  // branch's newest token, [nb][Hkv][d], and the pools they are written to;
+  // all null for a plain decode step.
+  const uint4* k_step;
+  const uint4* v_step;
+  uint4* k_pool;
+  uint4* v_pool;
 };
 
 // A work item read from the (caller-uploaded) plan must stay inside the

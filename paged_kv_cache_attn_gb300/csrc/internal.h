@@ -76,6 +76,19 @@ int launch_append_scatter(void* k_pool, void* v_pool, const void* k_new,
                           int Hkv, int d, int B, int n, int tok0,
                           const int32_t* dst_blocks, int n_dst,
                           void* stream);
+// One branch's run of a batched append: input rows [row, row + n) are the
+// branch's tokens tok0 .. tok0 + n - 1, landing in blocks dst[t / 16 -
+// first_lblock] (t = branch token index), slot t % 16.
+struct ScatterRun {
+  int32_t row, n, tok0, first_lblock;
+  std::vector<int32_t> dst;
+};
+// Scatter a batch of runs (input [L][total][Hkv][d]) in as few launches as
+// the kernel parameter space allows.
+int launch_append_batch(void* k_pool, void* v_pool, const void* k_new,
+                        const void* v_new, int64_t num_blocks, int L, int Hkv,
+                        int d, int32_t total, const std::vector<ScatterRun>& runs,
+                        void* stream);
 // Copy whole blocks src[i] -> dst[i] (every layer, K and V).
 int launch_block_copy(void* k_pool, void* v_pool, int64_t num_blocks, int L,
                       int Hkv, int d, int B, const int32_t* src,

@@ -206,6 +206,144 @@ extern "C" kv_status kv_append(kv_pool* p, int32_t id, int32_t n,
   return KV_OK;
 }
 
+// Blocks a batch of appends takes, in allocation order, and for each entry
+// the logical->physical map of the blocks its tokens land in.  Nothing is
+// changed; returns OOM / NOT_FOUND / INVALID_ARG like the single append.
+namespace {
+struct PlannedAppend {
+  int32_t id, n, tok0, first_lb;
+  std::vector<int32_t> dst;  // physical block of logical first_lb + i
+  int32_t fresh_begin, fresh_count;
+};
+}  // namespace
+
+static kv_status plan_appends(kv_pool* p, int32_t n, const int32_t* ids,
+                              const int32_t* n_tokens,
+                              std::vector<PlannedAppend>* out,
+                              std::vector<int32_t>* fresh) {
+  if (!p) return fail(KV_ERR_INVALID_ARG, "null pool");
+  if (n < 0 || (n > 0 && (!ids || !n_tokens)))
+    return fail(KV_ERR_INVALID_ARG, "bad batch arrays");
+  const int32_t B = p->block_size;
+  // Branch lengths and table sizes as the batch proceeds (a branch may
+  // appear more than once).
+  std::vector<std::pair<int32_t, std::pair<int32_t, int32_t>>> cur;  // id -> (len, nblk)
+  auto state = [&](int32_t id) -> std::pair<int32_t, int32_t>& {
+    for (auto& c : cur)
+      if (c.first == id) return c.second;
+    Node& nd = p->nodes[id];
+    cur.push_back({id, {nd.seq_len, (int32_t)nd.table.size()}});
+    return cur.back().second;
+  };
+  size_t next_free = 0;  // blocks taken so far from the top of the stack
+  for (int32_t i = 0; i < n; ++i) {
+    Node* nd;
+    if (kv_status s = get_live(p, ids[i], &nd)) return s;
+    if (n_tokens[i] < 0) return fail(KV_ERR_INVALID_ARG, "negative token count");
+    auto& st = state(ids[i]);
+    if ((int64_t)st.first + n_tokens[i] > (int64_t)INT32_MAX / 2)
+      return fail(KV_ERR_INVALID_ARG, "sequence too long");
+    if (st.first % B != 0 && st.second == (int32_t)nd->table.size() &&
+        p->ref[nd->table.back()] != 1)
+      return fail(KV_ERR_INTERNAL, "partial last block of branch %d is shared",
+                  ids[i]);
+    const int32_t need =
+        blocks_for((int64_t)st.first + n_tokens[i], B) - st.second;
+    if (next_free + (size_t)need > p->free_stack.size())
+      return fail(KV_ERR_OOM, "batch append needs more blocks than the %zu free",
+                  p->free_stack.size());
+    PlannedAppend pa{ids[i], n_tokens[i], st.first, st.first / B, {},
+                     (int32_t)next_free, need};
+    for (int32_t k = 0; k < need; ++k)
+      fresh->push_back(p->free_stack[p->free_stack.size() - 1 - next_free - k]);
+    if (n_tokens[i] > 0) {
+      const int32_t last_lb = (st.first + n_tokens[i] - 1) / B;
+      // Blocks of this branch in logical order: the committed table, then
+      // blocks taken earlier in this batch, then this entry's fresh blocks.
+      std::vector<int32_t> mine;
+      for (auto& q : *out)
+        if (q.id == ids[i])
+          for (int32_t k = 0; k < q.fresh_count; ++k)
+            mine.push_back((*fresh)[q.fresh_begin + k]);
+      for (int32_t lb = pa.first_lb; lb <= last_lb; ++lb) {
+        const int32_t tsz = (int32_t)nd->table.size();
+        int32_t blk;
+        if (lb < tsz)
+          blk = nd->table[lb];
+        else if (lb - tsz < (int32_t)mine.size())
+          blk = mine[lb - tsz];
+        else
+          blk = (*fresh)[next_free + (lb - tsz - (int32_t)mine.size())];
+        pa.dst.push_back(blk);
+      }
+    }
+    next_free += need;
+    st.first += n_tokens[i];
+    st.second += need;
+    out->push_back(std::move(pa));
+  }
+  return KV_OK;
+}
+
+static void commit_appends(kv_pool* p, const std::vector<PlannedAppend>& plan,
+                           const std::vector<int32_t>& fresh) {
+  for (const PlannedAppend& pa : plan) {
+    Node& nd = p->nodes[pa.id];
+    for (int32_t k = 0; k < pa.fresh_count; ++k) {
+      const int32_t b = fresh[pa.fresh_begin + k];
+      p->free_stack.pop_back();
+      p->ref[b] = 1;
+      nd.table.push_back(b);
+    }
+    nd.seq_len += pa.n;
+  }
+}
+
+extern "C" kv_status kv_reserve(kv_pool* p, int32_t n, const int32_t* ids,
+                                const int32_t* n_tokens) {
+  pkv::clear_error();
+  std::vector<PlannedAppend> plan;
+  std::vector<int32_t> fresh;
+  if (kv_status s = plan_appends(p, n, ids, n_tokens, &plan, &fresh)) return s;
+  commit_appends(p, plan, fresh);
+  return KV_OK;
+}
+
+extern "C" kv_status kv_append_batch(kv_pool* p, int32_t n, const int32_t* ids,
+                                     const int32_t* n_tokens,
+                                     const void* k_new, const void* v_new,
+                                     void* stream) {
+  pkv::clear_error();
+  std::vector<PlannedAppend> plan;
+  std::vector<int32_t> fresh;
+  if (kv_status s = plan_appends(p, n, ids, n_tokens, &plan, &fresh)) return s;
+  int64_t total = 0;
+  for (auto& pa : plan) total += pa.n;
+  if (total > INT32_MAX / 2) return fail(KV_ERR_INVALID_ARG, "batch too large");
+  if (p->has_data() && total > 0) {
+    if (!k_new || !v_new)
+      return fail(KV_ERR_INVALID_ARG, "k_new / v_new required for a data pool");
+    if (((uintptr_t)k_new | (uintptr_t)v_new) & 15)
+      return fail(KV_ERR_INVALID_ARG, "k_new / v_new must be 16-byte aligned");
+    std::vector<pkv::ScatterRun> runs;
+    int32_t row = 0;
+    for (auto& pa : plan) {
+      if (pa.n > 0)
+        runs.push_back({row, pa.n, pa.tok0, pa.first_lb, pa.dst});
+      row += pa.n;
+    }
+    int err = pkv::launch_append_batch(p->k_pool, p->v_pool, k_new, v_new,
+                                       p->num_blocks, p->num_layers,
+                                       p->num_kv_heads, p->head_dim,
+                                       (int32_t)total, runs, stream);
+    if (err) return fail(KV_ERR_CUDA, "batch append launch failed (cuda %d)", err);
+  } else if (!p->has_data() && (k_new || v_new)) {
+    return fail(KV_ERR_INVALID_ARG, "metadata-only pool takes no data");
+  }
+  commit_appends(p, plan, fresh);
+  return KV_OK;
+}
+
 extern "C" kv_status kv_fork_branches(kv_pool* p, int32_t parent, int32_t n,
                                       int32_t* out_children, void* stream) {
   pkv::clear_error();

@@ -10,6 +10,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <vector>
 
 #include "internal.h"
 
@@ -86,6 +87,50 @@ __global__ void block_copy_kernel(const __grid_constant__ CopyArgs a) {
   }
 }
 
+constexpr int kMaxRuns = 128;
+constexpr int kMaxRunDst = 1536;
+
+struct RunDesc {
+  int row, n, tok0, first_lb, dst_off;
+};
+
+struct BatchArgs {
+  uint4* k_pool;
+  uint4* v_pool;
+  const uint4* k_new;
+  const uint4* v_new;
+  int64_t num_blocks;
+  int L, Hkv, vec_per_row, total;
+  int n_runs;
+  RunDesc runs[kMaxRuns];
+  int dst[kMaxRunDst];
+};
+
+// blockIdx.y = run; grid-stride over (layer, token, head, vec) of that run.
+__global__ void append_batch_kernel(const __grid_constant__ BatchArgs a) {
+  const RunDesc r = a.runs[blockIdx.y];
+  const int64_t per_layer = (int64_t)r.n * a.Hkv * a.vec_per_row;
+  const int64_t work = per_layer * a.L;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < work;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t layer = i / per_layer;
+    int64_t rem = i - layer * per_layer;
+    const int vec = (int)(rem % a.vec_per_row);
+    rem /= a.vec_per_row;
+    const int h = (int)(rem % a.Hkv);
+    const int tok = (int)(rem / a.Hkv);
+    const int t = r.tok0 + tok;
+    const int blk = a.dst[r.dst_off + t / 16 - r.first_lb];
+    const int64_t src =
+        ((layer * a.total + r.row + tok) * a.Hkv + h) * (int64_t)a.vec_per_row + vec;
+    const int64_t dst =
+        (((layer * a.num_blocks + blk) * a.Hkv + h) * 16 + t % 16) *
+            (int64_t)a.vec_per_row + vec;
+    a.k_pool[dst] = a.k_new[src];
+    a.v_pool[dst] = a.v_new[src];
+  }
+}
+
 int grid_for(int64_t work) {
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
@@ -134,6 +179,61 @@ int launch_append_scatter(void* k_pool, void* v_pool, const void* k_new,
   }
   (void)n_dst;
   return 0;
+}
+
+int launch_append_batch(void* k_pool, void* v_pool, const void* k_new,
+                        const void* v_new, int64_t num_blocks, int L, int Hkv,
+                        int d, int32_t total, const std::vector<ScatterRun>& runs,
+                        void* stream) {
+  BatchArgs a;
+  a.k_pool = static_cast<uint4*>(k_pool);
+  a.v_pool = static_cast<uint4*>(v_pool);
+  a.k_new = static_cast<const uint4*>(k_new);
+  a.v_new = static_cast<const uint4*>(v_new);
+  a.num_blocks = num_blocks;
+  a.L = L;
+  a.Hkv = Hkv;
+  a.vec_per_row = d / 8;
+  a.total = total;
+  a.n_runs = 0;
+  int n_dst = 0;
+  int64_t max_work = 0;
+  auto flush = [&]() -> int {
+    if (a.n_runs == 0) return 0;
+    const int gx = std::max(1, std::min(grid_for(max_work), 64));
+    append_batch_kernel<<<dim3(gx, a.n_runs), 256, 0, (cudaStream_t)stream>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    a.n_runs = 0;
+    n_dst = 0;
+    max_work = 0;
+    return (int)e;
+  };
+  for (const ScatterRun& run : runs) {
+    // Split a run into pieces whose blocks fit the parameter space.
+    int tok = 0;
+    while (tok < run.n) {
+      const int t0 = run.tok0 + tok;
+      const int lb0 = t0 / 16;
+      const int lb_cap = lb0 + kMaxRunDst / 2 - 1;
+      const int tok_end = std::min(run.n, (lb_cap + 1) * 16 - run.tok0);
+      const int lb1 = (run.tok0 + tok_end - 1) / 16;
+      const int nb_piece = lb1 - lb0 + 1;
+      if (a.n_runs == kMaxRuns || n_dst + nb_piece > kMaxRunDst) {
+        if (int e = flush()) return e;
+      }
+      RunDesc& r = a.runs[a.n_runs++];
+      r.row = run.row + tok;
+      r.n = tok_end - tok;
+      r.tok0 = t0;
+      r.first_lb = lb0;
+      r.dst_off = n_dst;
+      for (int lb = lb0; lb <= lb1; ++lb)
+        a.dst[n_dst++] = run.dst[lb - run.first_lblock];
+      max_work = std::max<int64_t>(max_work, (int64_t)r.n * Hkv * (d / 8) * L);
+      tok = tok_end;
+    }
+  }
+  return flush();
 }
 
 int launch_block_copy(void* k_pool, void* v_pool, int64_t num_blocks, int L,

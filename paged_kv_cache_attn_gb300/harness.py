@@ -163,5 +163,22 @@ class Batch:
                             self.info, d["workspace"], d["workspace"].numel(),
                             stream, w.block_size)
 
+    def decode_append(self, q, k_step, v_step, out, layer: int = 0,
+                      stream=None):
+        """Decode step that also writes each branch's newest token (reserved
+        beforehand with kv_reserve): k_step, v_step device bf16 [nb][Hkv][d]."""
+        c = self.cache
+        w = c.w
+        if self.dev is None:
+            self.upload()
+        d = self.dev
+        B.paged_decode_append_attn(q, k_step, v_step, c.k[layer], c.v[layer],
+                                   w.num_blocks, d["tables"], d["seq_lens"],
+                                   d["groups"], len(self.groups), self.nb,
+                                   self.tables.shape[1], w.Hq, w.Hkv, w.d,
+                                   w.scale, out, d["plan"], self.info,
+                                   d["workspace"], d["workspace"].numel(),
+                                   stream, w.block_size)
+
     def device_status(self, stream=None):
         return B.kv_check_device_status(self.dev["workspace"], stream)

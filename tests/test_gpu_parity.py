@@ -177,3 +177,105 @@ def test_full_size_sampled_rows(built, name):
     # the largest |V| of a bf16 N(0,1) draw.
     assert np.isfinite(gpu).all() and np.abs(gpu).max() < 8
     cache.close()
+
+
+# ---- batched append and the fused append + decode step -----------------------
+
+def _bits_to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda() \
+        .view(torch.bfloat16)
+
+
+def test_batched_append_pool_bytes(built):
+    """Children's first segments appended in one kv_append_batch land where
+    the oracle's sequential appends put them."""
+    w = SMALL["fanout"]()
+    cache = H.Cache.__new__(H.Cache)
+    cache.w, cache.with_data, cache.device = w, True, "cuda"
+    shape = (w.num_layers, w.num_blocks, w.Hkv, w.block_size, w.d)
+    cache.k = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
+    cache.v = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
+    cache.h = B.kv_pool_create(w.num_blocks, w.num_layers, w.Hkv, w.d, cache.k,
+                               cache.v, w.initial_free_order())
+    pending = []                        # consecutive appends -> one batch
+
+    def flush():
+        if not pending:
+            return
+        ks, vs = zip(*[w.node_kv(i) for i in pending])
+        k = np.concatenate(ks, axis=1)
+        v = np.concatenate(vs, axis=1)
+        B.kv_append_batch(cache.h, pending,
+                          [w.nodes[i].n_tokens for i in pending],
+                          _bits_to_dev(k), _bits_to_dev(v))
+        pending.clear()
+
+    for op in w.ops:
+        if op[0] == "append":
+            pending.append(op[1])
+            continue
+        flush()
+        if op[0] == "create":
+            B.kv_branch_create(cache.h)
+        else:
+            B.kv_fork_branches(cache.h, op[1], op[2])
+    flush()
+    torch.cuda.synchronize()
+    ref = rp.replay(w, with_data=True)
+    k = bf16_bits(cache.k)
+    v = bf16_bits(cache.v)
+    for i, n in enumerate(ref.model.nodes):
+        t = np.arange(n.seq_len)
+        blk = np.asarray(n.table)[t // 16]
+        assert np.array_equal(k[:, blk, :, t % 16], ref.data.k[:, blk, :, t % 16])
+        assert np.array_equal(v[:, blk, :, t % 16], ref.data.v[:, blk, :, t % 16])
+    cache.close()
+
+
+@pytest.mark.parametrize("name", ["long_context", "deep_tree", "tiny_tree",
+                                  "fanout_3tiles"])
+def test_fused_append_decode(built, name):
+    """Each branch's newest token is reserved, then written and attended to in
+    one step; the result matches the oracle over the sequence with the token
+    appended, the slot holds the token, and a later plain step sees it."""
+    w = SMALL[name]()
+    cache = H.Cache(w)
+    ref = rp.replay(w, with_data=False)
+    ids = cache.decode_ids
+    nb = len(ids)
+    B.kv_reserve(cache.h, ids, [1] * nb)
+    rng = np.random.default_rng(9)
+    ks = W.f32_to_bf16_bits(rng.standard_normal((nb, w.Hkv, w.d), dtype=np.float32))
+    vs = W.f32_to_bf16_bits(rng.standard_normal((nb, w.Hkv, w.d), dtype=np.float32))
+    q = w.queries(nb, salt=5)
+    bt = cache.batch().upload()
+    out = torch.empty((nb, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+    bt.decode_append(_bits_to_dev(q), _bits_to_dev(ks), _bits_to_dev(vs), out)
+    torch.cuda.synchronize()
+    assert bt.device_status() == (0, 0)
+    gpu = att.bf16_to_f64(bf16_bits(out))
+    for b in range(nb):
+        k, v = ref.branch_kv(ids[b])
+        k = np.concatenate([k[0], ks[b][None]], axis=0)
+        v = np.concatenate([v[0], vs[b][None]], axis=0)
+        want = att.decode_branch_contiguous(q[b], k, v, w.Hkv, w.scale)
+        assert_close(gpu[b], want, f"{name} fused row {b}")
+    # The slot now holds the token.
+    kp, vp = bf16_bits(cache.k), bf16_bits(cache.v)
+    for b in range(nb):
+        L = int(bt.seq_lens[b])
+        blk = int(bt.tables[b][(L - 1) // 16])
+        assert np.array_equal(kp[0, blk, :, (L - 1) % 16], ks[b])
+        assert np.array_equal(vp[0, blk, :, (L - 1) % 16], vs[b])
+    # A plain step afterwards reads it from the pool.
+    q2 = w.queries(nb, salt=6)
+    out2 = torch.empty_like(out)
+    bt.decode(_bits_to_dev(q2), out2)
+    gpu2 = att.bf16_to_f64(bf16_bits(out2))
+    for b in range(min(nb, 6)):
+        k, v = ref.branch_kv(ids[b])
+        k = np.concatenate([k[0], ks[b][None]], axis=0)
+        v = np.concatenate([v[0], vs[b][None]], axis=0)
+        want = att.decode_branch_contiguous(q2[b], k, v, w.Hkv, w.scale)
+        assert_close(gpu2[b], want, f"{name} later row {b}")
+    cache.close()

@@ -327,3 +327,59 @@ def test_plan_rejects_bad_input():
                             [[0, 2, 0, 2], [0, 2, 1, 1]])
     plan, info = B.paged_decode_plan(2, 8, 2, 128, 4, [40, 40], [[0, 2, 0, 2]])
     assert info.partial_rows > 0 and len(plan) == info.plan_ints
+
+
+# ---- batched append and reservation ------------------------------------------
+
+@pytest.mark.parametrize("seed", range(4))
+def test_batched_append_equals_sequential(seed):
+    rnd = random.Random(100 + seed)
+    nblocks = 200
+    order = list(range(nblocks))
+    rnd.shuffle(order)
+    hb = B.kv_pool_create(nblocks, 1, 2, 64, None, None, order)
+    hr = B.kv_pool_create(nblocks, 1, 2, 64, None, None, order)
+    m = al.PoolModel(nblocks, 16, order)
+    roots = []
+    for _ in range(3):
+        roots.append(B.kv_branch_create(hb))
+        B.kv_branch_create(hr)
+        m.create()
+    for r in roots:
+        n = rnd.randint(1, 40)
+        B.kv_append(hb, r, n); B.kv_append(hr, r, n); m.append(r, n)
+    kids = B.kv_fork_branches(hb, roots[0], 3)
+    B.kv_fork_branches(hr, roots[0], 3)
+    m.fork_many(roots[0], 3)
+    ids = kids + roots + [kids[0]]          # a branch may repeat
+    n_tok = [rnd.randint(0, 35) for _ in ids]
+    B.kv_append_batch(hb, ids, n_tok)
+    B.kv_reserve(hr, ids, n_tok)
+    for i, n in zip(ids, n_tok):
+        m.append(i, n)
+    for h in (hb, hr):
+        assert B.kv_get_refcounts(h, nblocks).tolist() == m.ref
+        assert B.kv_get_free_stack(h).tolist() == m.free_stack()
+        for i in range(len(m.nodes)):
+            t, L = B.kv_get_block_table(h, i)
+            assert t.tolist() == m.nodes[i].table and L == m.nodes[i].seq_len
+    B.kv_pool_destroy(hb)
+    B.kv_pool_destroy(hr)
+
+
+def test_batched_append_is_all_or_nothing():
+    h = B.kv_pool_create(6, 1, 1, 64)
+    a = B.kv_branch_create(h)
+    b = B.kv_branch_create(h)
+    B.kv_append(h, a, 20)
+    before = (B.kv_get_refcounts(h, 6).tolist(), B.kv_get_free_stack(h).tolist())
+    with pytest.raises(B.KVError) as e:
+        B.kv_append_batch(h, [a, b], [20, 60])     # needs 1 + 4 > 4 free
+    assert e.value.code == B.KV_ERR_OOM
+    with pytest.raises(B.KVError) as e:
+        B.kv_reserve(h, [a, 99], [1, 1])
+    assert e.value.code == B.KV_ERR_NOT_FOUND
+    assert (B.kv_get_refcounts(h, 6).tolist(),
+            B.kv_get_free_stack(h).tolist()) == before
+    assert B.kv_get_block_table(h, a)[1] == 20
+    B.kv_pool_destroy(h)
