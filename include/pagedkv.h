@@ -181,6 +181,75 @@ kv_status kv_evict(kv_pool* pool, int32_t n, const int32_t* ids,
                    const double* scores, int32_t stop_kind, int64_t target,
                    int32_t* out_n_evicted, int32_t* out_evicted_ids);
 
+/* ---- radix prefix index (host) ------------------------------------------- */
+
+/* A token-keyed radix index over a pool ([DMW] RadixAttention section: a
+ * compressed prefix tree whose nodes hold a token sequence and its KV, a
+ * lock_ref pinning a node and all its ancestors while in use, and
+ * least-recently-used eviction of leaves whose lock_ref is zero).  The
+ * sharing unit is a full 16-token block: a node's key is a whole number of
+ * blocks and its value the physical block of each.  The index holds one
+ * reference on every block it stores.  Recency is a logical clock that ticks
+ * once per kv_radix_match / kv_radix_insert; every node on the matched path
+ * takes the current tick.  Node 0 is the root (empty key, never evicted).
+ * Node ids are assigned in creation order and never reused; a node split
+ * where a match ends inside it keeps its id for the deeper part and the new
+ * id names the prefix part.  Host-only; not thread-safe with the pool. */
+typedef struct kv_radix kv_radix;
+
+typedef struct kv_radix_node_t {
+  int32_t live;
+  int32_t parent;      /* -1 for the root */
+  int32_t n_blocks;    /* blocks (16 tokens each) of this node's key */
+  int32_t lock_ref;
+  int32_t n_children;
+  int32_t reserved;
+  int64_t last_access; /* logical clock of the last match / insert through it */
+} kv_radix_node_t;
+
+kv_status kv_radix_create(kv_pool* pool, kv_radix** out);
+/* Releases every block reference the index holds, then the index. */
+kv_status kv_radix_destroy(kv_radix* radix);
+
+/* Longest cached prefix of tokens[0 .. n_tokens) in whole blocks.  *out_node
+ * = deepest matched node (0 if none), *out_matched_tokens = 16 x matched
+ * blocks.  A match ending inside a node splits it. */
+kv_status kv_radix_match(kv_radix* radix, int32_t n_tokens,
+                         const int32_t* tokens, int32_t* out_node,
+                         int32_t* out_matched_tokens);
+
+/* Index branch `branch`'s KV under its token sequence tokens[0 .. n_tokens)
+ * (the caller's tokens of that branch, oldest first): the full blocks past
+ * the longest cached prefix become a new leaf holding the branch's physical
+ * blocks (+1 reference each).  *out_node = the node ending at the last full
+ * block.  Errors: NOT_FOUND (branch), INVALID_ARG. */
+kv_status kv_radix_insert(kv_radix* radix, int32_t branch, int32_t n_tokens,
+                          const int32_t* tokens, int32_t* out_node);
+
+/* New pool branch (a root: depth 0) whose table is the blocks on the path
+ * from the root to `node` (+1 reference each): a request starting from a
+ * cached prefix.  *out_branch = its handle. */
+kv_status kv_radix_fork(kv_radix* radix, int32_t node, int32_t* out_branch);
+
+/* lock_ref + 1 / - 1 on `node` and every ancestor (unlock: INVALID_ARG if any
+ * would go below 0). */
+kv_status kv_radix_lock(kv_radix* radix, int32_t node);
+kv_status kv_radix_unlock(kv_radix* radix, int32_t node);
+
+/* Evict leaves with lock_ref 0, least recently used first (ties: smaller
+ * id), releasing their blocks, until the pool has at least
+ * target_free_blocks free blocks or no leaf is evictable.  A parent left
+ * without children becomes a leaf in turn.  out_evicted (nullable) gets the
+ * ids in eviction order (room for kv_radix_num_nodes entries). */
+kv_status kv_radix_evict(kv_radix* radix, int64_t target_free_blocks,
+                         int32_t* out_n_evicted, int32_t* out_evicted);
+
+kv_status kv_radix_node_info(kv_radix* radix, int32_t node,
+                             kv_radix_node_t* out);
+kv_status kv_radix_node_blocks(kv_radix* radix, int32_t node, int32_t* out,
+                               int32_t cap, int32_t* out_n);
+kv_status kv_radix_num_nodes(kv_radix* radix, int32_t* out_n);
+
 /* ---- introspection (host) ----------------------------------------------- */
 
 kv_status kv_branch_info(kv_pool* pool, int32_t id, kv_branch_info_t* out);

@@ -187,6 +187,16 @@ class PoolModel:
     def fork(self, parent: int):
         return self.fork_many(parent, 1)[0]
 
+    def adopt(self, blocks) -> int:
+        """New root branch whose table is the given (full, cached) blocks,
+        +1 reference each: a request starting from a cached prefix."""
+        nd = Node(parent=-1, depth=0, table=list(blocks),
+                  seq_len=len(blocks) * self.block_size)
+        for b in blocks:
+            self.ref[b] += 1
+        self.nodes.append(nd)
+        return len(self.nodes) - 1
+
     def free_node(self, nid: int) -> None:
         nd = self.live_node(nid)
         for blk in nd.table:

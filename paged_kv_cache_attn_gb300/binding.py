@@ -66,6 +66,13 @@ class kv_decode_plan_info(C.Structure):
         return {f: getattr(self, f) for f, _ in self._fields_}
 
 
+class kv_radix_node_t(C.Structure):
+    _fields_ = [("live", C.c_int32), ("parent", C.c_int32),
+                ("n_blocks", C.c_int32), ("lock_ref", C.c_int32),
+                ("n_children", C.c_int32), ("reserved", C.c_int32),
+                ("last_access", C.c_int64)]
+
+
 _i32p = C.POINTER(C.c_int32)
 _i64p = C.POINTER(C.c_int64)
 _f64p = C.POINTER(C.c_double)
@@ -125,6 +132,19 @@ _SIGS = {
                                               C.POINTER(kv_decode_plan_info),
                                               _vp]),
     "kv_check_device_status": (C.c_int32, [_vp, _vp, _i32p, _i32p]),
+    "kv_radix_create": (C.c_int32, [_vp, C.POINTER(_vp)]),
+    "kv_radix_destroy": (C.c_int32, [_vp]),
+    "kv_radix_match": (C.c_int32, [_vp, C.c_int32, _i32p, _i32p, _i32p]),
+    "kv_radix_insert": (C.c_int32, [_vp, C.c_int32, C.c_int32, _i32p, _i32p]),
+    "kv_radix_fork": (C.c_int32, [_vp, C.c_int32, _i32p]),
+    "kv_radix_lock": (C.c_int32, [_vp, C.c_int32]),
+    "kv_radix_unlock": (C.c_int32, [_vp, C.c_int32]),
+    "kv_radix_evict": (C.c_int32, [_vp, C.c_int64, _i32p, _i32p]),
+    "kv_radix_node_info": (C.c_int32, [_vp, C.c_int32,
+                                       C.POINTER(kv_radix_node_t)]),
+    "kv_radix_node_blocks": (C.c_int32, [_vp, C.c_int32, _i32p, C.c_int32,
+                                         _i32p]),
+    "kv_radix_num_nodes": (C.c_int32, [_vp, _i32p]),
     "kv_set_launch_events": (C.c_int32, [C.POINTER(_vp), C.c_int32]),
     "kv_last_error": (C.c_char_p, []),
 }
@@ -446,3 +466,76 @@ def kv_set_launch_events(events):
     arr = (_vp * len(events))(*handles)
     _events_keepalive = arr
     _check(_lib.kv_set_launch_events(arr, len(events)))
+
+
+# ---- radix prefix index ------------------------------------------------------
+
+def kv_radix_create(pool):
+    h = _vp()
+    _check(_lib.kv_radix_create(pool, C.byref(h)))
+    return h
+
+
+def kv_radix_destroy(r):
+    _check(_lib.kv_radix_destroy(r))
+
+
+def kv_radix_match(r, tokens):
+    t = _i32(tokens)
+    node, n = C.c_int32(), C.c_int32()
+    _check(_lib.kv_radix_match(r, len(t), _as_i32p(t) if len(t) else None,
+                               C.byref(node), C.byref(n)))
+    return node.value, n.value
+
+
+def kv_radix_insert(r, branch, tokens):
+    t = _i32(tokens)
+    node = C.c_int32()
+    _check(_lib.kv_radix_insert(r, branch, len(t),
+                                _as_i32p(t) if len(t) else None,
+                                C.byref(node)))
+    return node.value
+
+
+def kv_radix_fork(r, node):
+    out = C.c_int32()
+    _check(_lib.kv_radix_fork(r, node, C.byref(out)))
+    return out.value
+
+
+def kv_radix_lock(r, node):
+    _check(_lib.kv_radix_lock(r, node))
+
+
+def kv_radix_unlock(r, node):
+    _check(_lib.kv_radix_unlock(r, node))
+
+
+def kv_radix_num_nodes(r):
+    out = C.c_int32()
+    _check(_lib.kv_radix_num_nodes(r, C.byref(out)))
+    return out.value
+
+
+def kv_radix_evict(r, target_free_blocks):
+    cap = max(kv_radix_num_nodes(r), 1)
+    out = np.zeros(cap, dtype=np.int32)
+    n = C.c_int32()
+    _check(_lib.kv_radix_evict(r, target_free_blocks, C.byref(n),
+                               _as_i32p(out)))
+    return out[:n.value].tolist()
+
+
+def kv_radix_node_info(r, node):
+    out = kv_radix_node_t()
+    _check(_lib.kv_radix_node_info(r, node, C.byref(out)))
+    return {f: getattr(out, f) for f, _ in out._fields_ if f != "reserved"}
+
+
+def kv_radix_node_blocks(r, node):
+    n = C.c_int32()
+    _check(_lib.kv_radix_node_blocks(r, node, None, 0, C.byref(n)))
+    out = np.zeros(max(n.value, 1), dtype=np.int32)
+    _check(_lib.kv_radix_node_blocks(r, node, _as_i32p(out), n.value,
+                                     C.byref(n)))
+    return out[:n.value].tolist()

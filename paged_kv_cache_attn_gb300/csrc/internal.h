@@ -8,6 +8,28 @@
 
 #include "pagedkv.h"
 
+// ---- pool state (host) -----------------------------------------------------
+struct Node {
+  int32_t parent = -1;
+  int32_t depth = 0;
+  int32_t seq_len = 0;
+  bool live = true;
+  std::vector<int32_t> table;
+  std::vector<int32_t> children;
+};
+
+struct kv_pool {
+  int64_t num_blocks = 0;
+  int32_t block_size = 16, num_layers = 1, num_kv_heads = 1, head_dim = 128;
+  void* k_pool = nullptr;
+  void* v_pool = nullptr;
+  std::vector<int32_t> ref;          // per block
+  std::vector<int32_t> free_stack;   // back() is handed out next
+  std::vector<Node> nodes;           // index = branch id
+
+  bool has_data() const { return k_pool != nullptr; }
+};
+
 namespace pkv {
 
 // ---- errors ---------------------------------------------------------------
