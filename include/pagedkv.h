@@ -181,6 +181,42 @@ kv_status kv_evict(kv_pool* pool, int32_t n, const int32_t* ids,
                    const double* scores, int32_t stop_kind, int64_t target,
                    int32_t* out_n_evicted, int32_t* out_evicted_ids);
 
+/* ---- host tier: spill and restore ([DMW] cross-tier memory offloading) ---- */
+
+/* Attach a host tier: caller-owned pinned host pools host_k / host_v with the
+ * device pool's layout ([num_layers][host_slots][Hkv][16][head_dim] bf16),
+ * reachable from the device (pinned memory under unified addressing), or
+ * both NULL for a metadata-only pool.  Free slots form a LIFO stack, slot 0
+ * handed out first.  Errors: INVALID_ARG (sizes, a second tier, pointers not
+ * matching the pool's kind). */
+kv_status kv_offload_attach(kv_pool* pool, void* host_k, void* host_v,
+                            int64_t host_slots);
+
+/* Move the blocks that branches ids[0..n) own alone (reference count 1) to
+ * host slots (taken in branch order, table order), copying every layer of K
+ * and V on `stream`, and free them on the device (pushed on the free stack
+ * in the same order); shared blocks stay on the device.  A spilled table
+ * entry reads -(slot + 2) in kv_get_block_table.  A branch holding spilled
+ * blocks cannot be appended to, forked, batched or indexed until
+ * kv_restore; kv_free releases its host slots.  Later device work that
+ * reuses the freed blocks must be ordered after `stream`.  *out_n_blocks
+ * (nullable) = blocks moved.  All or nothing.  Errors: NOT_FOUND,
+ * INVALID_ARG (no tier), OOM (host slots), CUDA. */
+kv_status kv_spill(kv_pool* pool, int32_t n, const int32_t* ids, void* stream,
+                   int32_t* out_n_blocks);
+
+/* Bring every spilled block of branches ids[0..n) (each listed once) back
+ * into device blocks popped from the free stack (branch order, table order),
+ * copying on `stream`, and return their host slots to the host free stack.
+ * All or nothing.  Errors: NOT_FOUND, INVALID_ARG, OOM (device blocks),
+ * CUDA. */
+kv_status kv_restore(kv_pool* pool, int32_t n, const int32_t* ids,
+                     void* stream, int32_t* out_n_blocks);
+
+/* Free host slots, next-to-be-handed-out first (host out[cap]). */
+kv_status kv_get_host_free(kv_pool* pool, int32_t* out, int64_t cap,
+                           int64_t* out_n);
+
 /* ---- radix prefix index (host) ------------------------------------------- */
 
 /* A token-keyed radix index over a pool ([DMW] RadixAttention section: a

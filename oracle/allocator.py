@@ -187,6 +187,61 @@ class PoolModel:
     def fork(self, parent: int):
         return self.fork_many(parent, 1)[0]
 
+    # -- host tier ("Dismantling the Memory Wall", cross-tier offloading) -------
+    # Reading taken: a branch's blocks that only it references move to host
+    # slots (a LIFO stack, slot 0 first) in branch order and table order and
+    # are freed on the device in that order; shared blocks stay.  A spilled
+    # table entry is -(slot + 2).  Restoring pops device blocks in branch and
+    # table order and pushes each host slot back as it is emptied.
+
+    def attach_host(self, slots: int) -> None:
+        self.host_free = list(reversed(range(slots)))
+
+    def host_free_stack(self) -> list:
+        return list(reversed(self.host_free))
+
+    def spill(self, ids) -> list:
+        """Returns the (device block, host slot) copies."""
+        moved, seen = [], set()
+        for i in ids:
+            for b in self.live_node(i).table:
+                if b >= 0 and self.ref[b] == 1 and b not in seen:
+                    seen.add(b)
+                    moved.append(b)
+        if len(moved) > len(self.host_free):
+            raise OutOfBlocks("host tier full")
+        pairs = []
+        for i in ids:
+            nd = self.nodes[i]
+            for j, b in enumerate(nd.table):
+                if len(pairs) < len(moved) and b == moved[len(pairs)]:
+                    slot = self.host_free.pop()
+                    self.ref[b] = 0
+                    self.free.append(b)
+                    nd.table[j] = -(slot + 2)
+                    pairs.append((b, slot))
+        return pairs
+
+    def restore(self, ids) -> list:
+        """Returns the (host slot, device block) copies."""
+        ids = list(ids)
+        if len(set(ids)) != len(ids):
+            raise ValueError("branch listed twice")
+        need = sum(1 for i in ids for b in self.live_node(i).table if b < 0)
+        if need > len(self.free):
+            raise OutOfBlocks("restore needs more device blocks")
+        pairs = []
+        for i in ids:
+            nd = self.nodes[i]
+            for j, b in enumerate(nd.table):
+                if b < 0:
+                    blk = self._pop()
+                    slot = -b - 2
+                    self.host_free.append(slot)
+                    nd.table[j] = blk
+                    pairs.append((slot, blk))
+        return pairs
+
     def adopt(self, blocks) -> int:
         """New root branch whose table is the given (full, cached) blocks,
         +1 reference each: a request starting from a cached prefix."""
@@ -200,6 +255,9 @@ class PoolModel:
     def free_node(self, nid: int) -> None:
         nd = self.live_node(nid)
         for blk in nd.table:
+            if blk < 0:                     # spilled: its host slot is freed
+                self.host_free.append(-blk - 2)
+                continue
             self._release(blk)
         nd.table = []
         nd.seq_len = 0
@@ -274,7 +332,8 @@ class PoolModel:
                 continue
             assert len(nd.table) == blocks_for(nd.seq_len, self.block_size)
             for blk in nd.table:
-                count[blk] += 1
+                if blk >= 0:
+                    count[blk] += 1
         assert count == self.ref
         assert len(set(self.free)) == len(self.free)
         assert sorted(self.free) == [b for b in range(self.num_blocks)

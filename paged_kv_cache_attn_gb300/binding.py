@@ -132,6 +132,10 @@ _SIGS = {
                                               C.POINTER(kv_decode_plan_info),
                                               _vp]),
     "kv_check_device_status": (C.c_int32, [_vp, _vp, _i32p, _i32p]),
+    "kv_offload_attach": (C.c_int32, [_vp, _vp, _vp, C.c_int64]),
+    "kv_spill": (C.c_int32, [_vp, C.c_int32, _i32p, _vp, _i32p]),
+    "kv_restore": (C.c_int32, [_vp, C.c_int32, _i32p, _vp, _i32p]),
+    "kv_get_host_free": (C.c_int32, [_vp, _i32p, C.c_int64, _i64p]),
     "kv_radix_create": (C.c_int32, [_vp, C.POINTER(_vp)]),
     "kv_radix_destroy": (C.c_int32, [_vp]),
     "kv_radix_match": (C.c_int32, [_vp, C.c_int32, _i32p, _i32p, _i32p]),
@@ -539,3 +543,33 @@ def kv_radix_node_blocks(r, node):
     _check(_lib.kv_radix_node_blocks(r, node, _as_i32p(out), n.value,
                                      C.byref(n)))
     return out[:n.value].tolist()
+
+
+# ---- host tier ----------------------------------------------------------------
+
+def kv_offload_attach(h, host_k, host_v, host_slots):
+    _check(_lib.kv_offload_attach(h, _ptr(host_k), _ptr(host_v), host_slots))
+
+
+def kv_spill(h, ids, stream=None) -> int:
+    ids = _i32(ids)
+    n = C.c_int32()
+    _check(_lib.kv_spill(h, len(ids), _as_i32p(ids), _stream(stream),
+                         C.byref(n)))
+    return n.value
+
+
+def kv_restore(h, ids, stream=None) -> int:
+    ids = _i32(ids)
+    n = C.c_int32()
+    _check(_lib.kv_restore(h, len(ids), _as_i32p(ids), _stream(stream),
+                           C.byref(n)))
+    return n.value
+
+
+def kv_get_host_free(h) -> np.ndarray:
+    n = C.c_int64()
+    _check(_lib.kv_get_host_free(h, None, 0, C.byref(n)))
+    out = np.zeros(max(n.value, 1), dtype=np.int32)
+    _check(_lib.kv_get_host_free(h, _as_i32p(out), n.value, C.byref(n)))
+    return out[:n.value]

@@ -14,6 +14,9 @@ struct Node {
   int32_t depth = 0;
   int32_t seq_len = 0;
   bool live = true;
+  int32_t spilled = 0;  // table entries held in the host tier
+  // Physical block ids; an entry -(slot + 2) is a block spilled to host slot
+  // `slot` (-1 stays free for batch-table padding).
   std::vector<int32_t> table;
   std::vector<int32_t> children;
 };
@@ -26,9 +29,19 @@ struct kv_pool {
   std::vector<int32_t> ref;          // per block
   std::vector<int32_t> free_stack;   // back() is handed out next
   std::vector<Node> nodes;           // index = branch id
+  // Host tier (kv_offload_attach): caller-owned pinned host pools with the
+  // device pool's layout, `host_slots` blocks each, and a LIFO stack of free
+  // slots (back() handed out next).
+  void* host_k = nullptr;
+  void* host_v = nullptr;
+  int64_t host_slots = 0;
+  std::vector<int32_t> host_free;
 
   bool has_data() const { return k_pool != nullptr; }
 };
+
+inline int32_t spill_code(int32_t slot) { return -(slot + 2); }
+inline int32_t spill_slot(int32_t code) { return -code - 2; }
 
 namespace pkv {
 
@@ -111,6 +124,15 @@ int launch_append_batch(void* k_pool, void* v_pool, const void* k_new,
                         const void* v_new, int64_t num_blocks, int L, int Hkv,
                         int d, int32_t total, const std::vector<ScatterRun>& runs,
                         void* stream);
+// Copy whole blocks between two pools of the same layout (every layer, K and
+// V): src block src[i] of a pool with src_blocks blocks -> dst block dst[i]
+// of a pool with dst_blocks blocks.  Either side may be pinned host memory
+// reachable from the device.
+int launch_block_transfer(const void* src_k, const void* src_v,
+                          int64_t src_blocks, void* dst_k, void* dst_v,
+                          int64_t dst_blocks, int L, int Hkv, int d,
+                          const int32_t* src, const int32_t* dst, int n,
+                          void* stream);
 // Copy whole blocks src[i] -> dst[i] (every layer, K and V).
 int launch_block_copy(void* k_pool, void* v_pool, int64_t num_blocks, int L,
                       int Hkv, int d, int B, const int32_t* src,

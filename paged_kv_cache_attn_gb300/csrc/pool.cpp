@@ -138,6 +138,8 @@ extern "C" kv_status kv_append(kv_pool* p, int32_t id, int32_t n,
   Node* nd;
   if (kv_status s = get_live(p, id, &nd)) return s;
   if (n < 0) return fail(KV_ERR_INVALID_ARG, "negative token count");
+  if (nd->spilled)
+    return fail(KV_ERR_INVALID_ARG, "branch %d is spilled: restore it first", id);
   if ((int64_t)nd->seq_len + n > (int64_t)INT32_MAX / 2)
     return fail(KV_ERR_INVALID_ARG, "sequence too long");
   const int32_t B = p->block_size;
@@ -220,6 +222,9 @@ static kv_status plan_appends(kv_pool* p, int32_t n, const int32_t* ids,
     Node* nd;
     if (kv_status s = get_live(p, ids[i], &nd)) return s;
     if (n_tokens[i] < 0) return fail(KV_ERR_INVALID_ARG, "negative token count");
+    if (nd->spilled)
+      return fail(KV_ERR_INVALID_ARG, "branch %d is spilled: restore it first",
+                  ids[i]);
     auto& st = state(ids[i]);
     if ((int64_t)st.first + n_tokens[i] > (int64_t)INT32_MAX / 2)
       return fail(KV_ERR_INVALID_ARG, "sequence too long");
@@ -331,6 +336,9 @@ extern "C" kv_status kv_fork_branches(kv_pool* p, int32_t parent, int32_t n,
   if (kv_status s = get_live(p, parent, &pn)) return s;
   if (n < 1 || !out_children)
     return fail(KV_ERR_INVALID_ARG, "fork count must be >= 1 with an output");
+  if (pn->spilled)
+    return fail(KV_ERR_INVALID_ARG, "branch %d is spilled: restore it first",
+                parent);
   if (p->nodes.size() + (size_t)n > (size_t)INT32_MAX)
     return fail(KV_ERR_INVALID_ARG, "branch id space exhausted");
   const int32_t B = p->block_size;
@@ -385,8 +393,13 @@ extern "C" kv_status kv_fork_branch(kv_pool* p, int32_t parent,
 
 static void release_node(kv_pool* p, Node& nd) {
   for (int32_t b : nd.table) {
+    if (b < 0) {
+      p->host_free.push_back(spill_slot(b));   // a spilled block's host slot
+      continue;
+    }
     if (--p->ref[b] == 0) p->free_stack.push_back(b);
   }
+  nd.spilled = 0;
   nd.table.clear();
   nd.table.shrink_to_fit();
   nd.seq_len = 0;
@@ -621,6 +634,9 @@ extern "C" kv_status kv_build_batch(kv_pool* p, int32_t nb, const int32_t* ids,
                   "%d", ids[b], nd->table.size(), max_blocks);
     if (nd->seq_len < 1)
       return fail(KV_ERR_INVALID_ARG, "branch %d is empty", ids[b]);
+    if (nd->spilled)
+      return fail(KV_ERR_INVALID_ARG, "branch %d is spilled: restore it first",
+                  ids[b]);
     rows[b] = nd;
   }
   const int32_t B = p->block_size;
@@ -653,5 +669,139 @@ extern "C" kv_status kv_build_batch(kv_pool* p, int32_t nb, const int32_t* ids,
   }
   std::copy(seg.begin(), seg.end(), groups);
   *out_n_groups = ng;
+  return KV_OK;
+}
+
+// ---- host tier: spill and restore ------------------------------------------
+// "Dismantling the Memory Wall", cross-tier offload: blocks leave HBM for
+// host memory instead of being dropped, and come back before use.
+
+extern "C" kv_status kv_offload_attach(kv_pool* p, void* host_k, void* host_v,
+                                       int64_t host_slots) {
+  pkv::clear_error();
+  if (!p) return fail(KV_ERR_INVALID_ARG, "null pool");
+  if (host_slots < 1 || host_slots > (int64_t)INT32_MAX / 2)
+    return fail(KV_ERR_INVALID_ARG, "host_slots out of range");
+  if ((host_k == nullptr) != (host_v == nullptr))
+    return fail(KV_ERR_INVALID_ARG, "host_k and host_v both set or both NULL");
+  if (p->has_data() != (host_k != nullptr))
+    return fail(KV_ERR_INVALID_ARG, "a data pool needs host buffers; a "
+                                    "metadata-only pool takes none");
+  if (((uintptr_t)host_k | (uintptr_t)host_v) & 15)
+    return fail(KV_ERR_INVALID_ARG, "host buffers must be 16-byte aligned");
+  if (p->host_slots > 0)
+    return fail(KV_ERR_INVALID_ARG, "a host tier is already attached");
+  p->host_k = host_k;
+  p->host_v = host_v;
+  p->host_slots = host_slots;
+  p->host_free.resize(host_slots);
+  for (int64_t i = 0; i < host_slots; ++i)
+    p->host_free[i] = (int32_t)(host_slots - 1 - i);  // slot 0 handed out first
+  return KV_OK;
+}
+
+extern "C" kv_status kv_spill(kv_pool* p, int32_t n, const int32_t* ids,
+                              void* stream, int32_t* out_n_blocks) {
+  pkv::clear_error();
+  if (!p) return fail(KV_ERR_INVALID_ARG, "null pool");
+  if (p->host_slots < 1) return fail(KV_ERR_INVALID_ARG, "no host tier attached");
+  if (n < 0 || (n > 0 && !ids)) return fail(KV_ERR_INVALID_ARG, "bad ids");
+  // Blocks owned by one branch alone go to the host; shared ones stay.
+  std::vector<int32_t> src, dst;
+  std::vector<char> taken(p->num_blocks, 0);
+  for (int32_t i = 0; i < n; ++i) {
+    Node* nd;
+    if (kv_status s = get_live(p, ids[i], &nd)) return s;
+    for (int32_t b : nd->table)
+      if (b >= 0 && p->ref[b] == 1 && !taken[b]) {
+        taken[b] = 1;
+        src.push_back(b);
+      }
+  }
+  if (src.size() > p->host_free.size())
+    return fail(KV_ERR_OOM, "spill needs %zu host slots, %zu free", src.size(),
+                p->host_free.size());
+  for (size_t k = 0; k < src.size(); ++k)
+    dst.push_back(p->host_free[p->host_free.size() - 1 - k]);
+  if (p->has_data() && !src.empty()) {
+    int err = pkv::launch_block_transfer(
+        p->k_pool, p->v_pool, p->num_blocks, p->host_k, p->host_v,
+        p->host_slots, p->num_layers, p->num_kv_heads, p->head_dim, src.data(),
+        dst.data(), (int)src.size(), stream);
+    if (err) return fail(KV_ERR_CUDA, "spill copy launch failed (cuda %d)", err);
+  }
+  // Commit in the same order the slots were taken.
+  size_t k = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    Node& nd = p->nodes[ids[i]];
+    for (int32_t& b : nd.table) {
+      if (b < 0 || k >= src.size() || src[k] != b) continue;
+      p->host_free.pop_back();
+      p->ref[b] = 0;
+      p->free_stack.push_back(b);
+      b = spill_code(dst[k]);
+      ++nd.spilled;
+      ++k;
+    }
+  }
+  if (out_n_blocks) *out_n_blocks = (int32_t)src.size();
+  return KV_OK;
+}
+
+extern "C" kv_status kv_restore(kv_pool* p, int32_t n, const int32_t* ids,
+                                void* stream, int32_t* out_n_blocks) {
+  pkv::clear_error();
+  if (!p) return fail(KV_ERR_INVALID_ARG, "null pool");
+  if (n < 0 || (n > 0 && !ids)) return fail(KV_ERR_INVALID_ARG, "bad ids");
+  std::vector<int32_t> src, dst;
+  for (int32_t i = 0; i < n; ++i) {
+    Node* nd;
+    if (kv_status s = get_live(p, ids[i], &nd)) return s;
+    for (int32_t j = 0; j < i; ++j)
+      if (ids[j] == ids[i])
+        return fail(KV_ERR_INVALID_ARG, "branch %d listed twice", ids[i]);
+    for (int32_t b : nd->table)
+      if (b < 0) src.push_back(spill_slot(b));
+  }
+  if (src.size() > p->free_stack.size())
+    return fail(KV_ERR_OOM, "restore needs %zu blocks, %zu free", src.size(),
+                p->free_stack.size());
+  for (size_t k = 0; k < src.size(); ++k)
+    dst.push_back(p->free_stack[p->free_stack.size() - 1 - k]);
+  if (p->has_data() && !src.empty()) {
+    int err = pkv::launch_block_transfer(
+        p->host_k, p->host_v, p->host_slots, p->k_pool, p->v_pool,
+        p->num_blocks, p->num_layers, p->num_kv_heads, p->head_dim, src.data(),
+        dst.data(), (int)src.size(), stream);
+    if (err)
+      return fail(KV_ERR_CUDA, "restore copy launch failed (cuda %d)", err);
+  }
+  size_t k = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    Node& nd = p->nodes[ids[i]];
+    for (int32_t& b : nd.table) {
+      if (b >= 0) continue;
+      p->free_stack.pop_back();
+      p->ref[dst[k]] = 1;
+      p->host_free.push_back(spill_slot(b));
+      b = dst[k];
+      ++k;
+    }
+    nd.spilled = 0;
+  }
+  if (out_n_blocks) *out_n_blocks = (int32_t)src.size();
+  return KV_OK;
+}
+
+extern "C" kv_status kv_get_host_free(kv_pool* p, int32_t* out, int64_t cap,
+                                      int64_t* out_n) {
+  pkv::clear_error();
+  if (!p) return fail(KV_ERR_INVALID_ARG, "null pool");
+  const int64_t n = (int64_t)p->host_free.size();
+  if (out_n) *out_n = n;
+  if (out) {
+    if (cap < n) return fail(KV_ERR_INVALID_ARG, "cap too small");
+    std::copy(p->host_free.rbegin(), p->host_free.rend(), out);
+  }
   return KV_OK;
 }

@@ -158,6 +158,9 @@ extern "C" kv_status kv_radix_insert(kv_radix* r, int32_t branch,
   if (branch < 0 || branch >= (int32_t)p->nodes.size() || !p->nodes[branch].live)
     return fail(KV_ERR_NOT_FOUND, "branch %d does not exist", branch);
   const Node& br = p->nodes[branch];
+  if (br.spilled)
+    return fail(KV_ERR_INVALID_ARG, "branch %d is spilled: restore it first",
+                branch);
   const int32_t nfull = std::min(n_tokens, br.seq_len) / kB;
   ++r->clock;
   auto [cur, pos] = walk(r, tokens, nfull);

@@ -87,6 +87,35 @@ __global__ void block_copy_kernel(const __grid_constant__ CopyArgs a) {
   }
 }
 
+struct XferArgs {
+  const uint4* src_k;
+  const uint4* src_v;
+  uint4* dst_k;
+  uint4* dst_v;
+  int64_t src_blocks, dst_blocks;
+  int L;
+  int vec_per_block;  // Hkv * 16 * d / 8 (one layer)
+  int n;
+  int src[kMaxDst / 2];
+  int dst[kMaxDst / 2];
+};
+
+__global__ void block_transfer_kernel(const __grid_constant__ XferArgs a) {
+  const int64_t per_pair = (int64_t)a.L * a.vec_per_block;
+  const int64_t total = per_pair * a.n;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int pair = (int)(i / per_pair);
+    const int64_t r = i - pair * per_pair;
+    const int64_t layer = r / a.vec_per_block;
+    const int64_t vec = r - layer * a.vec_per_block;
+    const int64_t s = (layer * a.src_blocks + a.src[pair]) * a.vec_per_block + vec;
+    const int64_t d = (layer * a.dst_blocks + a.dst[pair]) * a.vec_per_block + vec;
+    a.dst_k[d] = a.src_k[s];
+    a.dst_v[d] = a.src_v[s];
+  }
+}
+
 constexpr int kMaxRuns = 128;
 constexpr int kMaxRunDst = 1536;
 
@@ -234,6 +263,34 @@ int launch_append_batch(void* k_pool, void* v_pool, const void* k_new,
     }
   }
   return flush();
+}
+
+int launch_block_transfer(const void* src_k, const void* src_v,
+                          int64_t src_blocks, void* dst_k, void* dst_v,
+                          int64_t dst_blocks, int L, int Hkv, int d,
+                          const int32_t* src, const int32_t* dst, int n,
+                          void* stream) {
+  XferArgs a;
+  a.src_k = static_cast<const uint4*>(src_k);
+  a.src_v = static_cast<const uint4*>(src_v);
+  a.dst_k = static_cast<uint4*>(dst_k);
+  a.dst_v = static_cast<uint4*>(dst_v);
+  a.src_blocks = src_blocks;
+  a.dst_blocks = dst_blocks;
+  a.L = L;
+  a.vec_per_block = Hkv * 16 * d / 8;
+  for (int i0 = 0; i0 < n; i0 += kMaxDst / 2) {
+    a.n = std::min(n - i0, kMaxDst / 2);
+    for (int i = 0; i < a.n; ++i) {
+      a.src[i] = src[i0 + i];
+      a.dst[i] = dst[i0 + i];
+    }
+    const int64_t work = (int64_t)a.n * L * a.vec_per_block;
+    block_transfer_kernel<<<grid_for(work), 256, 0, (cudaStream_t)stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+  }
+  return 0;
 }
 
 int launch_block_copy(void* k_pool, void* v_pool, int64_t num_blocks, int L,
