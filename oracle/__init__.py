@@ -16,6 +16,13 @@ The oracle is deliberately plain and slow:
   partial block, free, and eviction ordered by the importance score
   omega = branch_score / (depth + 1) ("The Reasoning Engine Meltdown", §5 and
   §6; RKSC summary, §2.C RSBCM).
+* :mod:`oracle.fp8` -- FP8 (E4M3) KV storage: the element format from its
+  definition, one power-of-two scale per (block, kv-head) and tensor, block
+  writes with re-encoding when the scale grows, and decode over the
+  dequantised values (a reading: the pages only name FP8 KV quantisation,
+  "The Reasoning Engine Meltdown", §9).
+* :mod:`oracle.radix` -- the token-keyed radix prefix index ("Dismantling the
+  Memory Wall", RadixAttention section).
 * :mod:`oracle.brute` -- a scalar pure-Python restatement used only on tiny
   inputs as an extra cross-check of the vectorised code.
 
@@ -28,5 +35,7 @@ Parity pins (tests/test_oracle_*.py): closed forms (L = 1, identical keys,
 a dominant key, two-token sigmoid), invariants (physical-block permutation,
 shared vs private prefix layout, key-order permutation, score shift, linearity
 in V), the pages' KV-size worked example, the pages' page-table diagram and
-the allocator rules.  No oracle function is "parity unpinned".
+the allocator rules; for FP8, PyTorch's independent float8_e4m3fn type, hand-worked
+codes, the scale's defining inequalities, the 3-bit-mantissa error bound and a
+derived bound on the attention output.  No oracle function is "parity unpinned".
 """

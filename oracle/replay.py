@@ -16,15 +16,20 @@ import numpy as np
 
 from . import attention as att
 from .allocator import STOP_EVICTED_LEAVES, PoolData, PoolModel
+from .fp8 import Fp8PoolData, decode_step_fp8
 
 
 class Replayed:
-    def __init__(self, w, with_data: bool):
+    def __init__(self, w, with_data: bool, kv_dtype: str = "bf16"):
         self.w = w
+        self.kv_dtype = kv_dtype
         self.model = PoolModel(w.num_blocks, w.block_size,
                                w.initial_free_order())
-        self.data = (PoolData(w.num_layers, w.num_blocks, w.Hkv, w.block_size,
-                              w.d) if with_data else None)
+        if kv_dtype not in ("bf16", "e4m3"):
+            raise ValueError(kv_dtype)
+        kind = PoolData if kv_dtype == "bf16" else Fp8PoolData
+        self.data = (kind(w.num_layers, w.num_blocks, w.Hkv, w.block_size,
+                          w.d) if with_data else None)
         # logical[nid] = list of (source node, lo, hi): the node's tokens are
         # tokens [lo, hi) of the source node's own appended rows, in order.
         self.logical: dict[int, list] = {}
@@ -49,8 +54,10 @@ class Replayed:
         return np.concatenate(ks, axis=1), np.concatenate(vs, axis=1)
 
 
-def replay(w, with_data: bool = True) -> Replayed:
-    r = Replayed(w, with_data)
+def replay(w, with_data: bool = True, kv_dtype: str = "bf16") -> Replayed:
+    """``kv_dtype``: "bf16" (pool copy of bf16 bits) or "e4m3" (FP8 codes and
+    per-block scales, ``oracle.fp8``)."""
+    r = Replayed(w, with_data, kv_dtype)
     m = r.model
     own_appended = {}
     for op in w.ops:
@@ -104,5 +111,8 @@ def decode_all_from_pool(r: Replayed, q: np.ndarray, scale: float) -> np.ndarray
     m = r.model
     tables = [m.nodes[i].table for i in r.decode_ids]
     lens = [m.nodes[i].seq_len for i in r.decode_ids]
+    if r.kv_dtype == "e4m3":
+        return decode_step_fp8(q, r.data, tables, lens, scale,
+                               r.w.block_size)
     return att.decode_step(q, r.data.k[0], r.data.v[0], tables, lens, scale,
                            r.w.block_size)
