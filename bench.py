@@ -60,6 +60,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--fused-steps", type=int, default=30)
     ap.add_argument("--offload-branches", type=int, default=32)
+    ap.add_argument("--e4m3-steps", type=int, default=300)
     return ap.parse_args()
 
 
@@ -96,9 +97,11 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def unique_kv_bytes(tables, seq_lens, Hkv, d):
+def unique_kv_bytes(tables, seq_lens, Hkv, d, elem=2, record=0):
     """Distinct physical blocks read in the step, each weighted by the valid
-    tokens in it, times Hkv * d * 2 bytes * 2 (K and V)."""
+    tokens in it, times Hkv * d * elem bytes * 2 (K and V); plus `record`
+    bytes per distinct (block, kv-head) (the scale records of an e4m3
+    pool)."""
     valid = {}
     for row, L in zip(tables, seq_lens):
         nblk = (int(L) + 15) // 16
@@ -106,12 +109,14 @@ def unique_kv_bytes(tables, seq_lens, Hkv, d):
             n = min(16, int(L) - 16 * j)
             b = int(row[j])
             valid[b] = max(valid.get(b, 0), n)
-    return sum(valid.values()) * Hkv * d * 2 * 2
+    return (sum(valid.values()) * Hkv * d * elem * 2 +
+            len(valid) * Hkv * record)
 
 
-def item_bytes(plan, info, Hkv, d, seq_lens, which):
+def item_bytes(plan, info, Hkv, d, seq_lens, which, elem=2, record=0):
     """Algorithmic KV bytes one launch of a kernel reads: for each of its work
-    items, the valid tokens of its block range x 2 (K, V) x d x 2 bytes.  The
+    items, the valid tokens of its block range x 2 (K, V) x d x elem bytes,
+    plus `record` bytes per block of the range (e4m3 scale records).  The
     two CTAs of a tile-kernel cluster share one read of their common range
     (TMA multicast), so a pair counts once."""
     off = 16 if which == "row" else 16 + 8 * info.n_row_items
@@ -119,13 +124,14 @@ def item_bytes(plan, info, Hkv, d, seq_lens, which):
     items = plan[off:off + 8 * n].reshape(-1, 8)
     if which == "tile" and info.tile_cluster > 1:
         items = items[::info.tile_cluster]
-    tot = 0
+    tot = blocks = 0
     for b0, g, row0, nr, lo, hi, pb, masked in items:
         toks = (hi - lo) * 16
         if masked:
             toks = min(toks, int(seq_lens[b0]) - 16 * lo)
         tot += toks
-    return int(tot) * 2 * d * 2
+        blocks += hi - lo
+    return int(tot) * 2 * d * elem + int(blocks) * record
 
 
 class ClockSampler:
@@ -546,6 +552,64 @@ def run_ours(args):
                         "pinned host memory; best of 3",
             }
 
+    # NEXT-3: the same step over an e4m3 copy of the workload's pool (codes
+    # plus one 16-byte scale record per block and kv-head).
+    e4m3 = None
+    if args.e4m3_steps > 0:
+        c8 = H.Cache(w, device=dev, kv_dtype="e4m3")
+        b8 = c8.batch().upload()
+        uniq8 = unique_kv_bytes(b8.tables, b8.seq_lens, w.Hkv, w.d, elem=1,
+                                record=16)
+        for _ in range(3):
+            b8.decode(q, out)
+        torch.cuda.synchronize()
+        K8 = args.e4m3_steps
+        ev8 = [[torch.cuda.Event(enable_timing=True) for _ in range(6)]
+               for _ in range(K8)]
+        for row in ev8:
+            for e in row:
+                e.record(stream)
+        torch.cuda.synchronize()
+        s8 = torch.cuda.Event(enable_timing=True)
+        t8 = torch.cuda.Event(enable_timing=True)
+        s8.record(stream)
+        for i in range(K8):
+            B.kv_set_launch_events(ev8[i])
+            b8.decode(q, out)
+        t8.record(stream)
+        B.kv_set_launch_events(None)
+        torch.cuda.synchronize()
+        code8, det8 = b8.device_status()
+        if code8:
+            raise RuntimeError(f"e4m3 device status {code8} ({det8})")
+        ms8 = s8.elapsed_time(t8) / K8
+        split8 = sum(e[2].elapsed_time(e[3]) for e in ev8) / K8
+        merge8 = sum(e[4].elapsed_time(e[5]) for e in ev8) / K8
+        alg8 = item_bytes(b8.plan, b8.info, w.Hkv, w.d, b8.seq_lens, "row",
+                          elem=1, record=16)
+        ach8 = alg8 / (split8 / 1e3) / 1e9
+        e4m3 = {
+            "ms_per_step": round(ms8, 5),
+            "unique_kv_bytes": uniq8,
+            "value": round(uniq8 / (ms8 / 1e3) / 1e9, 1),
+            "unit": "GB/s (unique e4m3 KV bytes / step time)",
+            "branch_queries_per_s": round(nb / (ms8 / 1e3), 1),
+            "speedup_vs_bf16_step": round(ms_step / ms8, 3),
+            "kernels_ms": {"splitkv_e4m3": round(split8, 5),
+                           "lse_merge": round(merge8, 5)},
+            "roofline": {
+                "kernel": "splitkv_e4m3_kernel", "bound": "hbm",
+                "achieved": round(ach8, 1), "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": round(ach8 / peak, 4),
+                "algorithmic_bytes_per_launch": alg8,
+                "note": "every segment row tile re-reads its blocks (no "
+                        "e4m3 tensor-core tile kernel yet); bytes counted "
+                        "per item"},
+            "steps": K8,
+        }
+        c8.close()
+
     res = None
     if rank == 0:
         clocks = clk.summary()
@@ -606,6 +670,7 @@ def run_ours(args):
             "fused_append": fused,
             "radix_index": radix_timing(),
             "offload": offload,
+            "kv_e4m3": e4m3,
             "gpu_launches": launches_per_step * K,
             "clocks": clocks,
         }

@@ -29,6 +29,9 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Device work is asynchronous on that stream.
  *   - bf16 means IEEE bfloat16 (16-bit storage).
+ *   - e4m3 means the 8-bit floating-point format with a sign bit, 4 exponent
+ *     bits (bias 7) and 3 mantissa bits, no infinities, NaN = S.1111.111,
+ *     largest finite magnitude 448 (exponent field 0: subnormals m/8 * 2^-6).
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -60,6 +63,12 @@ typedef int32_t kv_status;
                                      (mma.sync) kernel, never tcgen05 */
 #define KV_PLAN_IGNORE_GROUPS 2   /* treat every branch as unshared (each
                                      branch re-reads its whole table) */
+#define KV_PLAN_KV_E4M3 4         /* the step reads an e4m3 pool
+                                     (paged_decode_attn_e4m3) */
+
+/* Element type of a pool's K and V. */
+#define KV_DTYPE_BF16 0
+#define KV_DTYPE_E4M3 1
 
 typedef struct kv_pool kv_pool; /* opaque */
 
@@ -69,7 +78,7 @@ typedef struct kv_pool_desc {
   int32_t num_layers;   /* >= 1 */
   int32_t num_kv_heads; /* Hkv >= 1 */
   int32_t head_dim;     /* d: 64 or 128 */
-  /* Device pools, caller-owned, each
+  /* Device pools, caller-owned, each (bf16 pools)
    * [num_layers][num_blocks][num_kv_heads][block_size][head_dim] bf16,
    * 16-byte aligned.  Both NULL: a metadata-only pool (the allocator, tables
    * and eviction run; appends and forks move no data). */
@@ -78,6 +87,29 @@ typedef struct kv_pool_desc {
   /* Host, nullable: a permutation of 0..num_blocks-1; element 0 is the first
    * block handed out.  NULL: ascending ids.  Copied; not retained. */
   const int32_t* initial_free_order;
+  /* KV_DTYPE_BF16 (layout above) or KV_DTYPE_E4M3.  An e4m3 pool stores
+   * each (layer, block, kv-head) K tile and V tile as 16 * head_dim e4m3
+   * codes (k_pool, v_pool: [num_layers][num_blocks][num_kv_heads][16 *
+   * head_dim] bytes) and one 16-byte scale record per (layer, block,
+   * kv-head) in kv_scales ([num_layers][num_blocks][num_kv_heads] x
+   * {float k_scale, float v_scale, 2 reserved words}, device, 16-byte
+   * aligned).  Stored value = code value * scale; each scale is a power of
+   * two 2^e, e in [-126, 120], the smallest with max|x| <= 448 * 2^e over
+   * the tile's values (nothing saturates).  Byte order inside a tile, token
+   * slot t, dimension c (0 <= c < head_dim):
+   *   K: t * head_dim + c, except that for head_dim 128 the 16-byte chunk
+   *      c / 16 of row t sits at chunk position (c / 16) ^ (t % 8);
+   *   V: ((c / 4) * 4 + t / 4) * 16 + (c % 4) * 4 + t % 4 (16-byte units of
+   *      4 dimensions x 4 tokens, dimension-major inside a unit).
+   * Writes quantise on the device: a write that starts a block (slot 0)
+   * takes the scale of its own rows; a later write keeps the block's scale
+   * unless its rows need a larger one, in which case the rows already
+   * stored are re-encoded from their stored values under the new scale.
+   * Each value is coded as the nearest e4m3 value of x / scale, ties to the
+   * even mantissa.  Non-finite inputs give unspecified codes.  kv_scales
+   * must be NULL for bf16 pools and for metadata-only pools. */
+  int32_t kv_dtype;
+  void* kv_scales;
 } kv_pool_desc;
 
 typedef struct kv_branch_info_t {
@@ -113,7 +145,9 @@ kv_status kv_branch_create(kv_pool* pool, int32_t* out_id);
  * all or nothing; then copies the new rows into their slots on `stream`.
  * k_new, v_new: device, [num_layers][n_tokens][num_kv_heads][head_dim] bf16,
  * 16-byte aligned, read before the stream passes the copy; NULL for a
- * metadata-only pool.  The partial last block being written is always owned
+ * metadata-only pool.  An e4m3 pool quantises the rows on the device under
+ * the block rule of kv_pool_desc (the appended rows of one block form one
+ * write).  The partial last block being written is always owned
  * by this branch alone (forks copy it), so no other branch sees the write.
  * Errors: NOT_FOUND, OOM (state unchanged), INVALID_ARG, CUDA. */
 kv_status kv_append(kv_pool* pool, int32_t id, int32_t n_tokens,
@@ -124,7 +158,8 @@ kv_status kv_append(kv_pool* pool, int32_t id, int32_t n_tokens,
  * (same blocks, same order), all or nothing over the whole batch.
  * k_new, v_new: device [num_layers][total][num_kv_heads][head_dim] bf16 with
  * total = sum(n_tokens); branch i's rows are rows sum(n_tokens[0..i)) + 0 ..
- * n_tokens[i]-1.  ids, n_tokens: host.  A branch may appear more than once.
+ * n_tokens[i]-1.  ids, n_tokens: host.  A branch may appear more than once
+ * (an e4m3 pool applies the writes to one block in list order).
  * Errors: NOT_FOUND, OOM (no change), INVALID_ARG, CUDA. */
 kv_status kv_append_batch(kv_pool* pool, int32_t n, const int32_t* ids,
                           const int32_t* n_tokens, const void* k_new,
@@ -183,14 +218,15 @@ kv_status kv_evict(kv_pool* pool, int32_t n, const int32_t* ids,
 
 /* ---- host tier: spill and restore ([DMW] cross-tier memory offloading) ---- */
 
-/* Attach a host tier: caller-owned pinned host pools host_k / host_v with the
- * device pool's layout ([num_layers][host_slots][Hkv][16][head_dim] bf16),
- * reachable from the device (pinned memory under unified addressing), or
- * both NULL for a metadata-only pool.  Free slots form a LIFO stack, slot 0
- * handed out first.  Errors: INVALID_ARG (sizes, a second tier, pointers not
- * matching the pool's kind). */
+/* Attach a host tier: caller-owned pinned host pools host_k / host_v (and,
+ * for an e4m3 pool, host_scales) with the device pools' layouts and
+ * host_slots blocks each ([num_layers][host_slots][Hkv][...]), reachable
+ * from the device (pinned memory under unified addressing), or all NULL for
+ * a metadata-only pool.  host_scales must be NULL for a bf16 pool.  Free
+ * slots form a LIFO stack, slot 0 handed out first.  Errors: INVALID_ARG
+ * (sizes, a second tier, pointers not matching the pool's kind). */
 kv_status kv_offload_attach(kv_pool* pool, void* host_k, void* host_v,
-                            int64_t host_slots);
+                            void* host_scales, int64_t host_slots);
 
 /* Move the blocks that branches ids[0..n) own alone (reference count 1) to
  * host slots (taken in branch order, table order), copying every layer of K
@@ -348,7 +384,7 @@ typedef struct kv_decode_plan_info {
   int32_t tile_cluster;    /* CTAs per cluster of the tcgen05 kernel (1 or 2):
                               with 2, the two 128-row tiles of one segment
                               share every K/V load (TMA multicast) */
-  int32_t reserved;
+  int32_t flags;           /* the KV_PLAN_* flags the plan was made with */
 } kv_decode_plan_info;
 
 /* Host half of a decode step: split the step into work items.
@@ -420,6 +456,39 @@ kv_status paged_decode_append_attn(
     const void* v_pool, int64_t num_blocks, const int32_t* block_tables,
     const int32_t* seq_lens, const int32_t* prefix_groups, int32_t n_groups,
     int32_t nb, int32_t max_blocks, int32_t Hq, int32_t Hkv, int32_t head_dim,
+    int32_t block_size, float scale, void* out, const int32_t* plan,
+    const kv_decode_plan_info* info, void* workspace, size_t ws_bytes,
+    void* stream);
+
+/* Decode attention over an e4m3 pool (kv_pool_desc.kv_dtype =
+ * KV_DTYPE_E4M3): the same result as paged_decode_attn computed from the
+ * stored values (code value x the tile's scale), with q and out bf16 as
+ * there.  k_pool, v_pool, kv_scales: this layer's base pointers of the
+ * e4m3 pool (layouts under kv_pool_desc).  The plan must be made with
+ * KV_PLAN_KV_E4M3 (and a bf16 step's plan without it).  Arithmetic: the
+ * codes are widened to f16 exactly, q is carried in f16 after a per-row
+ * power-of-two scaling (so nothing overflows), products accumulate in fp32.
+ * Errors and status reporting: as paged_decode_attn. */
+kv_status paged_decode_attn_e4m3(
+    const void* q, const void* k_pool, const void* v_pool,
+    const void* kv_scales, int64_t num_blocks, const int32_t* block_tables,
+    const int32_t* seq_lens, const int32_t* prefix_groups, int32_t n_groups,
+    int32_t nb, int32_t max_blocks, int32_t Hq, int32_t Hkv, int32_t head_dim,
+    int32_t block_size, float scale, void* out, const int32_t* plan,
+    const kv_decode_plan_info* info, void* workspace, size_t ws_bytes,
+    void* stream);
+
+/* paged_decode_append_attn for an e4m3 pool: first quantises each branch's
+ * newest token (k_step, v_step bf16 [nb][Hkv][head_dim]) into its reserved
+ * slot under the block rule above (one launch, writes to distinct blocks),
+ * then runs paged_decode_attn_e4m3 over the pool, on `stream`.  Errors: as
+ * paged_decode_attn. */
+kv_status paged_decode_append_attn_e4m3(
+    const void* q, const void* k_step, const void* v_step, const void* k_pool,
+    const void* v_pool, void* kv_scales, int64_t num_blocks,
+    const int32_t* block_tables, const int32_t* seq_lens,
+    const int32_t* prefix_groups, int32_t n_groups, int32_t nb,
+    int32_t max_blocks, int32_t Hq, int32_t Hkv, int32_t head_dim,
     int32_t block_size, float scale, void* out, const int32_t* plan,
     const kv_decode_plan_info* info, void* workspace, size_t ws_bytes,
     void* stream);

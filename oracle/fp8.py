@@ -185,6 +185,37 @@ class Fp8PoolData:
         return k, v
 
 
+def quantize_sequence(seg_lens, rows_bits: np.ndarray) -> np.ndarray:
+    """Stored (dequantised) values of one branch's logical token sequence.
+
+    ``rows_bits``: bf16 bits [L][T][Hkv][d] of the branch's tokens, oldest
+    first; ``seg_lens``: the lengths of the appends that wrote them, in order
+    (they sum to T).  Token t sits in the branch's logical block t // 16;
+    each append writes its tokens of every block it touches as one write, in
+    append order, and a block's first write starts at slot 0 -- also for a
+    copy-on-write block, whose copy carries the parent's codes and scale.
+    Returns float64 [L][T][Hkv][d].  Needs no pool, so it runs for a few
+    sampled branches of any workload."""
+    x = att.bf16_to_f64(rows_bits)
+    L, T, Hkv, d = x.shape
+    bounds = np.cumsum([0] + [int(n) for n in seg_lens])
+    if bounds[-1] != T:
+        raise ValueError("segment lengths do not add up to the sequence")
+    out = np.empty_like(x)
+    for lb in range((T + 15) // 16):
+        lo, hi = 16 * lb, min(16 * lb + 16, T)
+        writes = [(max(a, lo) - lo, min(b, hi) - lo)
+                  for a, b in zip(bounds[:-1], bounds[1:]) if a < hi and b > lo]
+        for layer in range(L):
+            for h in range(Hkv):
+                codes = np.zeros((16, d), np.uint8)
+                e = 0
+                for s0, s1 in writes:
+                    e = block_write(codes, e, s0, x[layer, lo + s0:lo + s1, h])
+                out[layer, lo:hi, h] = decode(codes[:hi - lo]) * 2.0 ** e
+    return out
+
+
 def gather_values(pool_f64: np.ndarray, table, seq_len: int, kv_head: int,
                   block_size: int) -> np.ndarray:
     """Like ``attention.gather_branch`` for a pool already in float64."""

@@ -30,6 +30,9 @@ KV_STOP_FREE_BLOCKS = 0
 KV_STOP_EVICTED_LEAVES = 1
 KV_PLAN_NO_TENSOR_CORES = 1
 KV_PLAN_IGNORE_GROUPS = 2
+KV_PLAN_KV_E4M3 = 4
+KV_DTYPE_BF16 = 0
+KV_DTYPE_E4M3 = 1
 
 _NAMES = {0: "OK", 1: "OOM", 2: "INVALID_ARG", 3: "NOT_FOUND", 4: "CUDA",
           5: "DEVICE", 6: "TIMEOUT", 7: "INTERNAL"}
@@ -46,7 +49,8 @@ class kv_pool_desc(C.Structure):
                 ("num_layers", C.c_int32), ("num_kv_heads", C.c_int32),
                 ("head_dim", C.c_int32), ("k_pool", C.c_void_p),
                 ("v_pool", C.c_void_p),
-                ("initial_free_order", C.POINTER(C.c_int32))]
+                ("initial_free_order", C.POINTER(C.c_int32)),
+                ("kv_dtype", C.c_int32), ("kv_scales", C.c_void_p)]
 
 
 class kv_branch_info_t(C.Structure):
@@ -60,7 +64,7 @@ class kv_decode_plan_info(C.Structure):
                 ("partial_rows", C.c_int64), ("n_row_items", C.c_int32),
                 ("n_tile_items", C.c_int32), ("n_merge_rows", C.c_int32),
                 ("chunk_blocks", C.c_int32), ("tile_cluster", C.c_int32),
-                ("reserved", C.c_int32)]
+                ("flags", C.c_int32)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -131,8 +135,24 @@ _SIGS = {
                                               _vp, _vp,
                                               C.POINTER(kv_decode_plan_info),
                                               _vp]),
+    "paged_decode_attn_e4m3": (C.c_int32, [_vp, _vp, _vp, _vp, C.c_int64, _vp,
+                                           _vp, _vp, C.c_int32, C.c_int32,
+                                           C.c_int32, C.c_int32, C.c_int32,
+                                           C.c_int32, C.c_int32, C.c_float,
+                                           _vp, _vp,
+                                           C.POINTER(kv_decode_plan_info),
+                                           _vp, C.c_size_t, _vp]),
+    "paged_decode_append_attn_e4m3": (C.c_int32, [_vp, _vp, _vp, _vp, _vp, _vp,
+                                                  C.c_int64, _vp, _vp, _vp,
+                                                  C.c_int32, C.c_int32,
+                                                  C.c_int32, C.c_int32,
+                                                  C.c_int32, C.c_int32,
+                                                  C.c_int32, C.c_float, _vp,
+                                                  _vp,
+                                                  C.POINTER(kv_decode_plan_info),
+                                                  _vp, C.c_size_t, _vp]),
     "kv_check_device_status": (C.c_int32, [_vp, _vp, _i32p, _i32p]),
-    "kv_offload_attach": (C.c_int32, [_vp, _vp, _vp, C.c_int64]),
+    "kv_offload_attach": (C.c_int32, [_vp, _vp, _vp, _vp, C.c_int64]),
     "kv_spill": (C.c_int32, [_vp, C.c_int32, _i32p, _vp, _i32p]),
     "kv_restore": (C.c_int32, [_vp, C.c_int32, _i32p, _vp, _i32p]),
     "kv_get_host_free": (C.c_int32, [_vp, _i32p, C.c_int64, _i64p]),
@@ -213,11 +233,12 @@ def _as_i32p(a: np.ndarray):
 
 def kv_pool_create(num_blocks, num_layers, num_kv_heads, head_dim,
                    k_pool=None, v_pool=None, initial_free_order=None,
-                   block_size=16):
+                   block_size=16, kv_dtype=KV_DTYPE_BF16, kv_scales=None):
     order = None if initial_free_order is None else _i32(initial_free_order)
     d = kv_pool_desc(num_blocks, block_size, num_layers, num_kv_heads,
                      head_dim, _ptr(k_pool), _ptr(v_pool),
-                     None if order is None else _as_i32p(order))
+                     None if order is None else _as_i32p(order), kv_dtype,
+                     _ptr(kv_scales))
     h = _vp()
     _check(_lib.kv_pool_create(C.byref(d), C.byref(h)))
     return h
@@ -432,6 +453,32 @@ def paged_decode_append_attn(q, k_step, v_step, k_pool, v_pool, num_blocks,
         _stream(stream)))
 
 
+def paged_decode_attn_e4m3(q, k_pool, v_pool, kv_scales, num_blocks,
+                           block_tables, seq_lens, prefix_groups, n_groups, nb,
+                           max_blocks, Hq, Hkv, head_dim, scale, out, plan,
+                           info, workspace, ws_bytes, stream=None,
+                           block_size=16):
+    _check(_lib.paged_decode_attn_e4m3(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(kv_scales), num_blocks,
+        _ptr(block_tables), _ptr(seq_lens), _ptr(prefix_groups), n_groups, nb,
+        max_blocks, Hq, Hkv, head_dim, block_size, scale, _ptr(out),
+        _ptr(plan), C.byref(info), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def paged_decode_append_attn_e4m3(q, k_step, v_step, k_pool, v_pool,
+                                  kv_scales, num_blocks, block_tables,
+                                  seq_lens, prefix_groups, n_groups, nb,
+                                  max_blocks, Hq, Hkv, head_dim, scale, out,
+                                  plan, info, workspace, ws_bytes,
+                                  stream=None, block_size=16):
+    _check(_lib.paged_decode_append_attn_e4m3(
+        _ptr(q), _ptr(k_step), _ptr(v_step), _ptr(k_pool), _ptr(v_pool),
+        _ptr(kv_scales), num_blocks, _ptr(block_tables), _ptr(seq_lens),
+        _ptr(prefix_groups), n_groups, nb, max_blocks, Hq, Hkv, head_dim,
+        block_size, scale, _ptr(out), _ptr(plan), C.byref(info),
+        _ptr(workspace), ws_bytes, _stream(stream)))
+
+
 def paged_decode_attn_noalloc(q, k_pool, v_pool, num_blocks, block_tables,
                               seq_lens, prefix_groups, n_groups, nb,
                               max_blocks, Hq, Hkv, head_dim, scale, out, plan,
@@ -547,8 +594,9 @@ def kv_radix_node_blocks(r, node):
 
 # ---- host tier ----------------------------------------------------------------
 
-def kv_offload_attach(h, host_k, host_v, host_slots):
-    _check(_lib.kv_offload_attach(h, _ptr(host_k), _ptr(host_v), host_slots))
+def kv_offload_attach(h, host_k, host_v, host_slots, host_scales=None):
+    _check(_lib.kv_offload_attach(h, _ptr(host_k), _ptr(host_v),
+                                  _ptr(host_scales), host_slots))
 
 
 def kv_spill(h, ids, stream=None) -> int:

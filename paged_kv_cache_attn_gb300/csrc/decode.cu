@@ -486,6 +486,11 @@ cudaError_t launch_merge(const MergeParams& mp, cudaStream_t stream) {
 
 }  // namespace
 
+// Split-KV kernel over an e4m3 pool; defined in decode_e4m3.cu.
+cudaError_t launch_split_e4m3(const SplitParams& sp, const void* k8,
+                              const void* v8, const void* scales, int n_items,
+                              int d, cudaStream_t stream);
+
 // Tensor-core (tcgen05) kernel for 128-row tiles; defined in decode_tc.cu.
 cudaError_t launch_tile_items(const CUtensorMap& tk, const CUtensorMap& tv,
                               const SplitParams& sp, const WorkItem* items,
@@ -548,14 +553,23 @@ extern "C" kv_status kv_set_launch_events(void* const* events,
   return KV_OK;
 }
 
+// The newest tokens an e4m3 step quantises into the pool before attending
+// (paged_decode_append_attn_e4m3).
+struct E4m3Append {
+  const void* k_step;
+  const void* v_step;
+  void* kv_scales;
+};
+
 static kv_status decode_impl(
     const void* q, const void* k_step, const void* v_step, const void* k_pool,
-    const void* v_pool, int64_t num_blocks, const int32_t* block_tables,
+    const void* v_pool, const void* kv_scales, int64_t num_blocks,
+    const int32_t* block_tables,
     const int32_t* seq_lens, const int32_t* prefix_groups, int32_t n_groups,
     int32_t nb, int32_t max_blocks, int32_t Hq, int32_t Hkv, int32_t d,
     int32_t block_size, float scale, void* out, const int32_t* plan,
     const kv_decode_plan_info* info, void* workspace, size_t ws_bytes,
-    void* stream) {
+    void* stream, const E4m3Append* pre = nullptr) {
   (void)prefix_groups;
   if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out ||
       !plan || !info || !workspace)
@@ -568,8 +582,16 @@ static kv_status decode_impl(
   if (block_size != 16) return fail(KV_ERR_INVALID_ARG, "block_size must be 16");
   if (num_blocks < 1 || num_blocks * Hkv * 16 > (int64_t)INT32_MAX)
     return fail(KV_ERR_INVALID_ARG, "num_blocks out of range");
-  if (((uintptr_t)q | (uintptr_t)k_pool | (uintptr_t)v_pool | (uintptr_t)out) & 15)
+  if (((uintptr_t)q | (uintptr_t)k_pool | (uintptr_t)v_pool | (uintptr_t)out |
+       (uintptr_t)kv_scales) & 15)
     return fail(KV_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned");
+  const bool e4m3 = kv_scales != nullptr;
+  if (e4m3 != ((info->flags & KV_PLAN_KV_E4M3) != 0))
+    return fail(KV_ERR_INVALID_ARG, e4m3 ? "an e4m3 step needs a plan made "
+                                           "with KV_PLAN_KV_E4M3"
+                                         : "plan was made for an e4m3 pool");
+  if (e4m3 && info->n_tile_items != 0)
+    return fail(KV_ERR_INVALID_ARG, "e4m3 plan with tensor-core tiles");
   if ((uintptr_t)workspace & 255)
     return fail(KV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   if (!std::isfinite(scale) || !(scale > 0.f))
@@ -584,8 +606,10 @@ static kv_status decode_impl(
   cudaStream_t st = (cudaStream_t)stream;
   CUtensorMap tk, tv;
   const int64_t rows = num_blocks * Hkv * 16;
-  if (kv_status s = pkv::make_pool_map(&tk, k_pool, rows, d)) return s;
-  if (kv_status s = pkv::make_pool_map(&tv, v_pool, rows, d)) return s;
+  if (!e4m3) {
+    if (kv_status s = pkv::make_pool_map(&tk, k_pool, rows, d)) return s;
+    if (kv_status s = pkv::make_pool_map(&tv, v_pool, rows, d)) return s;
+  }
 
   auto* ws = static_cast<uint8_t*>(workspace);
   pkv::SplitParams sp;
@@ -617,6 +641,14 @@ static kv_status decode_impl(
 
   cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(pkv::DeviceStatus), st);
   if (e != cudaSuccess) return fail(KV_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+  if (pre) {
+    const int err = pkv::launch_append_step_e4m3(
+        const_cast<void*>(k_pool), const_cast<void*>(v_pool), pre->kv_scales,
+        num_blocks, Hkv, d, block_tables, seq_lens, nb, max_blocks,
+        pre->k_step, pre->v_step, sp.status, st);
+    if (err)
+      return fail(KV_ERR_CUDA, "e4m3 append launch failed (cuda %d)", err);
+  }
   // With both passes present the tile pass forks onto the side stream and
   // joins back before the merge.
   pkv::SideStream* side = nullptr;
@@ -646,8 +678,12 @@ static kv_status decode_impl(
   if (info->n_row_items > 0) {
     sp.items = reinterpret_cast<const pkv::WorkItem*>(plan + off_row);
     pkv::mark(2, st);
-    e = d == 128 ? pkv::launch_split<128>(tk, tv, sp, info->n_row_items, st)
-                 : pkv::launch_split<64>(tk, tv, sp, info->n_row_items, st);
+    if (e4m3)
+      e = pkv::launch_split_e4m3(sp, k_pool, v_pool, kv_scales,
+                                 info->n_row_items, d, st);
+    else
+      e = d == 128 ? pkv::launch_split<128>(tk, tv, sp, info->n_row_items, st)
+                   : pkv::launch_split<64>(tk, tv, sp, info->n_row_items, st);
     pkv::mark(3, st);
     if (e != cudaSuccess)
       return fail(KV_ERR_CUDA, "split-KV kernel: %s", cudaGetErrorString(e));
@@ -684,10 +720,49 @@ extern "C" kv_status paged_decode_attn(
     const kv_decode_plan_info* info, void* workspace, size_t ws_bytes,
     void* stream) {
   pkv::clear_error();
-  return decode_impl(q, nullptr, nullptr, k_pool, v_pool, num_blocks,
+  return decode_impl(q, nullptr, nullptr, k_pool, v_pool, nullptr, num_blocks,
                      block_tables, seq_lens, prefix_groups, n_groups, nb,
                      max_blocks, Hq, Hkv, d, block_size, scale, out, plan, info,
                      workspace, ws_bytes, stream);
+}
+
+extern "C" kv_status paged_decode_attn_e4m3(
+    const void* q, const void* k_pool, const void* v_pool,
+    const void* kv_scales, int64_t num_blocks, const int32_t* block_tables,
+    const int32_t* seq_lens, const int32_t* prefix_groups, int32_t n_groups,
+    int32_t nb, int32_t max_blocks, int32_t Hq, int32_t Hkv, int32_t d,
+    int32_t block_size, float scale, void* out, const int32_t* plan,
+    const kv_decode_plan_info* info, void* workspace, size_t ws_bytes,
+    void* stream) {
+  pkv::clear_error();
+  if (!kv_scales) return fail(KV_ERR_INVALID_ARG, "kv_scales required");
+  return decode_impl(q, nullptr, nullptr, k_pool, v_pool, kv_scales,
+                     num_blocks, block_tables, seq_lens, prefix_groups,
+                     n_groups, nb, max_blocks, Hq, Hkv, d, block_size, scale,
+                     out, plan, info, workspace, ws_bytes, stream);
+}
+
+extern "C" kv_status paged_decode_append_attn_e4m3(
+    const void* q, const void* k_step, const void* v_step, const void* k_pool,
+    const void* v_pool, void* kv_scales, int64_t num_blocks,
+    const int32_t* block_tables, const int32_t* seq_lens,
+    const int32_t* prefix_groups, int32_t n_groups, int32_t nb,
+    int32_t max_blocks, int32_t Hq, int32_t Hkv, int32_t d,
+    int32_t block_size, float scale, void* out, const int32_t* plan,
+    const kv_decode_plan_info* info, void* workspace, size_t ws_bytes,
+    void* stream) {
+  pkv::clear_error();
+  if (!k_step || !v_step || !kv_scales)
+    return fail(KV_ERR_INVALID_ARG, "k_step, v_step and kv_scales required");
+  if (((uintptr_t)k_step | (uintptr_t)v_step) & 15)
+    return fail(KV_ERR_INVALID_ARG, "k_step / v_step must be 16-byte aligned");
+  if (nb > 65535 * 64 || Hkv > 65535)
+    return fail(KV_ERR_INVALID_ARG, "nb or Hkv too large for the append grid");
+  const E4m3Append pre{k_step, v_step, kv_scales};
+  return decode_impl(q, nullptr, nullptr, k_pool, v_pool, kv_scales,
+                     num_blocks, block_tables, seq_lens, prefix_groups,
+                     n_groups, nb, max_blocks, Hq, Hkv, d, block_size, scale,
+                     out, plan, info, workspace, ws_bytes, stream, &pre);
 }
 
 extern "C" kv_status paged_decode_append_attn(
@@ -703,7 +778,7 @@ extern "C" kv_status paged_decode_append_attn(
     return fail(KV_ERR_INVALID_ARG, "k_step / v_step required");
   if (((uintptr_t)k_step | (uintptr_t)v_step) & 15)
     return fail(KV_ERR_INVALID_ARG, "k_step / v_step must be 16-byte aligned");
-  return decode_impl(q, k_step, v_step, k_pool, v_pool, num_blocks,
+  return decode_impl(q, k_step, v_step, k_pool, v_pool, nullptr, num_blocks,
                      block_tables, seq_lens, prefix_groups, n_groups, nb,
                      max_blocks, Hq, Hkv, d, block_size, scale, out, plan, info,
                      workspace, ws_bytes, stream);

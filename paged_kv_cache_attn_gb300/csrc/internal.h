@@ -26,6 +26,8 @@ struct kv_pool {
   int32_t block_size = 16, num_layers = 1, num_kv_heads = 1, head_dim = 128;
   void* k_pool = nullptr;
   void* v_pool = nullptr;
+  int32_t kv_dtype = KV_DTYPE_BF16;
+  void* kv_scales = nullptr;         // e4m3: 16-byte record per (layer, block, head)
   std::vector<int32_t> ref;          // per block
   std::vector<int32_t> free_stack;   // back() is handed out next
   std::vector<Node> nodes;           // index = branch id
@@ -34,10 +36,18 @@ struct kv_pool {
   // slots (back() handed out next).
   void* host_k = nullptr;
   void* host_v = nullptr;
+  void* host_scales = nullptr;
   int64_t host_slots = 0;
   std::vector<int32_t> host_free;
 
   bool has_data() const { return k_pool != nullptr; }
+  bool e4m3() const { return kv_dtype == KV_DTYPE_E4M3; }
+  // Bytes of one (layer, block) in each of the K and V pools, and in the
+  // scale pool (0 for bf16).
+  int64_t tile_bytes() const {
+    return (int64_t)num_kv_heads * 16 * head_dim * (e4m3() ? 1 : 2);
+  }
+  int64_t scale_bytes() const { return e4m3() ? (int64_t)num_kv_heads * 16 : 0; }
 };
 
 inline int32_t spill_code(int32_t slot) { return -(slot + 2); }
@@ -124,18 +134,36 @@ int launch_append_batch(void* k_pool, void* v_pool, const void* k_new,
                         const void* v_new, int64_t num_blocks, int L, int Hkv,
                         int d, int32_t total, const std::vector<ScatterRun>& runs,
                         void* stream);
-// Copy whole blocks between two pools of the same layout (every layer, K and
-// V): src block src[i] of a pool with src_blocks blocks -> dst block dst[i]
-// of a pool with dst_blocks blocks.  Either side may be pinned host memory
-// reachable from the device.
-int launch_block_transfer(const void* src_k, const void* src_v,
-                          int64_t src_blocks, void* dst_k, void* dst_v,
-                          int64_t dst_blocks, int L, int Hkv, int d,
-                          const int32_t* src, const int32_t* dst, int n,
-                          void* stream);
-// Copy whole blocks src[i] -> dst[i] (every layer, K and V).
-int launch_block_copy(void* k_pool, void* v_pool, int64_t num_blocks, int L,
-                      int Hkv, int d, int B, const int32_t* src,
+// One side of a block move: the K, V (and scale, or null) buffers of a pool
+// holding `blocks` blocks per layer.  May be pinned host memory reachable
+// from the device.
+struct PoolBufs {
+  const void* k;
+  const void* v;
+  const void* s;
+  int64_t blocks;
+};
+// Copy whole blocks (every layer; K, V and scale records): block src[i] of
+// `from` -> block dst[i] of `to`.  kv_bytes / s_bytes: bytes of one (layer,
+// block) in each K/V buffer and in the scale buffer (multiples of 16).
+int launch_block_move(const PoolBufs& from, const PoolBufs& to, int L,
+                      int64_t kv_bytes, int64_t s_bytes, const int32_t* src,
                       const int32_t* dst, int n, void* stream);
+// Quantising append into an e4m3 pool: the runs' rows (input bf16
+// [L][total][Hkv][d]) are written block by block under the pool's block
+// rule; writes to one block are applied in run order.
+int launch_append_e4m3(void* k8, void* v8, void* scales, int64_t num_blocks,
+                       int L, int Hkv, int d, const void* k_new,
+                       const void* v_new, int32_t total,
+                       const std::vector<ScatterRun>& runs, void* stream);
+// One layer's newest token of every branch (k_step, v_step bf16
+// [nb][Hkv][d]) quantised into slot seq_lens[b] - 1 of its block; bad table
+// entries are recorded in `status` and skipped.
+int launch_append_step_e4m3(void* k8, void* v8, void* scales,
+                            int64_t num_blocks, int Hkv, int d,
+                            const int32_t* tables, const int32_t* seq_lens,
+                            int nb, int max_blocks, const void* k_step,
+                            const void* v_step, DeviceStatus* status,
+                            void* stream);
 
 }  // namespace pkv

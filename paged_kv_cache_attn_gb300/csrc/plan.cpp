@@ -77,9 +77,14 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   std::vector<int32_t> shared_end(nb, 0);
   std::vector<Unit> units;
   const bool use_groups = !(flags & KV_PLAN_IGNORE_GROUPS);
-  // The tcgen05 tile kernel is built for head_dim 128.
+  if (flags & ~(KV_PLAN_NO_TENSOR_CORES | KV_PLAN_IGNORE_GROUPS |
+                KV_PLAN_KV_E4M3))
+    return fail(KV_ERR_INVALID_ARG, "unknown plan flags 0x%x", flags);
+  // The tcgen05 tile kernel is built for bf16 pools with head_dim 128; e4m3
+  // steps run every unit through the split-KV kernel.
   const bool allow_tc = pkv::kTensorCoreKernel && d == 128 &&
-                        !(flags & KV_PLAN_NO_TENSOR_CORES);
+                        !(flags & KV_PLAN_NO_TENSOR_CORES) &&
+                        !(flags & KV_PLAN_KV_E4M3);
   if (use_groups && n_groups > 0) {
     std::vector<std::vector<std::pair<int32_t, int32_t>>> per_row(nb);
     for (int32_t i = 0; i < n_groups; ++i) {
@@ -216,7 +221,7 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   info->n_merge_rows = nb;
   info->chunk_blocks = chunk_rows;
   info->tile_cluster = tile_cluster;
-  info->reserved = 0;
+  info->flags = flags;
   if (!plan) return KV_OK;
   if (plan_cap < total)
     return fail(KV_ERR_INVALID_ARG, "plan_cap %lld < %lld", (long long)plan_cap,

@@ -81,6 +81,17 @@ extern "C" kv_status kv_pool_create(const kv_pool_desc* d, kv_pool** out) {
                                     "both be NULL");
   if (((uintptr_t)d->k_pool | (uintptr_t)d->v_pool) & 15)
     return fail(KV_ERR_INVALID_ARG, "pools must be 16-byte aligned");
+  if (d->kv_dtype != KV_DTYPE_BF16 && d->kv_dtype != KV_DTYPE_E4M3)
+    return fail(KV_ERR_INVALID_ARG, "kv_dtype must be KV_DTYPE_BF16 or "
+                                    "KV_DTYPE_E4M3, got %d", d->kv_dtype);
+  if (d->kv_dtype == KV_DTYPE_E4M3 && d->k_pool != nullptr) {
+    if (d->kv_scales == nullptr)
+      return fail(KV_ERR_INVALID_ARG, "an e4m3 data pool needs kv_scales");
+    if ((uintptr_t)d->kv_scales & 15)
+      return fail(KV_ERR_INVALID_ARG, "kv_scales must be 16-byte aligned");
+  } else if (d->kv_scales != nullptr) {
+    return fail(KV_ERR_INVALID_ARG, "kv_scales is only for e4m3 data pools");
+  }
   // Rows of one layer must fit a 2-D TMA coordinate (int32).
   if (d->num_blocks * d->num_kv_heads * d->block_size > (int64_t)INT32_MAX)
     return fail(KV_ERR_INVALID_ARG, "pool too large for one layer's rows");
@@ -92,6 +103,8 @@ extern "C" kv_status kv_pool_create(const kv_pool_desc* d, kv_pool** out) {
   p->head_dim = d->head_dim;
   p->k_pool = d->k_pool;
   p->v_pool = d->v_pool;
+  p->kv_dtype = d->kv_dtype;
+  p->kv_scales = d->kv_scales;
   p->ref.assign(d->num_blocks, 0);
   std::vector<int32_t> order(d->num_blocks);
   if (d->initial_free_order) {
@@ -173,10 +186,19 @@ extern "C" kv_status kv_append(kv_pool* p, int32_t id, int32_t n,
                                ? nd->table[lb]
                                : fresh[lb - (int32_t)nd->table.size()];
     }
-    int err = pkv::launch_append_scatter(
-        p->k_pool, p->v_pool, k_new, v_new, p->num_blocks, p->num_layers,
-        p->num_kv_heads, p->head_dim, B, n, nd->seq_len, dst.data(),
-        (int)dst.size(), stream);
+    int err;
+    if (p->e4m3()) {
+      std::vector<pkv::ScatterRun> runs{{0, n, nd->seq_len, first_lb, dst}};
+      err = pkv::launch_append_e4m3(p->k_pool, p->v_pool, p->kv_scales,
+                                    p->num_blocks, p->num_layers,
+                                    p->num_kv_heads, p->head_dim, k_new, v_new,
+                                    n, runs, stream);
+    } else {
+      err = pkv::launch_append_scatter(
+          p->k_pool, p->v_pool, k_new, v_new, p->num_blocks, p->num_layers,
+          p->num_kv_heads, p->head_dim, B, n, nd->seq_len, dst.data(),
+          (int)dst.size(), stream);
+    }
     if (err) return fail(KV_ERR_CUDA, "append copy launch failed (cuda %d)", err);
   }
   for (int32_t b : fresh) {
@@ -317,7 +339,13 @@ extern "C" kv_status kv_append_batch(kv_pool* p, int32_t n, const int32_t* ids,
         runs.push_back({row, pa.n, pa.tok0, pa.first_lb, pa.dst});
       row += pa.n;
     }
-    int err = pkv::launch_append_batch(p->k_pool, p->v_pool, k_new, v_new,
+    int err =
+        p->e4m3()
+            ? pkv::launch_append_e4m3(p->k_pool, p->v_pool, p->kv_scales,
+                                      p->num_blocks, p->num_layers,
+                                      p->num_kv_heads, p->head_dim, k_new,
+                                      v_new, (int32_t)total, runs, stream)
+            : pkv::launch_append_batch(p->k_pool, p->v_pool, k_new, v_new,
                                        p->num_blocks, p->num_layers,
                                        p->num_kv_heads, p->head_dim,
                                        (int32_t)total, runs, stream);
@@ -354,10 +382,11 @@ extern "C" kv_status kv_fork_branches(kv_pool* p, int32_t parent, int32_t n,
       dst.push_back(p->free_stack[p->free_stack.size() - 1 - i]);
     }
     if (p->has_data()) {
-      int err = pkv::launch_block_copy(p->k_pool, p->v_pool, p->num_blocks,
-                                       p->num_layers, p->num_kv_heads,
-                                       p->head_dim, B, src.data(), dst.data(),
-                                       n, stream);
+      const pkv::PoolBufs dev{p->k_pool, p->v_pool, p->kv_scales,
+                              p->num_blocks};
+      int err = pkv::launch_block_move(dev, dev, p->num_layers,
+                                       p->tile_bytes(), p->scale_bytes(),
+                                       src.data(), dst.data(), n, stream);
       if (err)
         return fail(KV_ERR_CUDA, "copy-on-write launch failed (cuda %d)", err);
     }
@@ -677,7 +706,7 @@ extern "C" kv_status kv_build_batch(kv_pool* p, int32_t nb, const int32_t* ids,
 // host memory instead of being dropped, and come back before use.
 
 extern "C" kv_status kv_offload_attach(kv_pool* p, void* host_k, void* host_v,
-                                       int64_t host_slots) {
+                                       void* host_scales, int64_t host_slots) {
   pkv::clear_error();
   if (!p) return fail(KV_ERR_INVALID_ARG, "null pool");
   if (host_slots < 1 || host_slots > (int64_t)INT32_MAX / 2)
@@ -687,12 +716,16 @@ extern "C" kv_status kv_offload_attach(kv_pool* p, void* host_k, void* host_v,
   if (p->has_data() != (host_k != nullptr))
     return fail(KV_ERR_INVALID_ARG, "a data pool needs host buffers; a "
                                     "metadata-only pool takes none");
-  if (((uintptr_t)host_k | (uintptr_t)host_v) & 15)
+  if (((uintptr_t)host_k | (uintptr_t)host_v | (uintptr_t)host_scales) & 15)
     return fail(KV_ERR_INVALID_ARG, "host buffers must be 16-byte aligned");
+  if ((host_scales != nullptr) != (p->has_data() && p->e4m3()))
+    return fail(KV_ERR_INVALID_ARG, "host_scales is required for an e4m3 data "
+                                    "pool and must be NULL otherwise");
   if (p->host_slots > 0)
     return fail(KV_ERR_INVALID_ARG, "a host tier is already attached");
   p->host_k = host_k;
   p->host_v = host_v;
+  p->host_scales = host_scales;
   p->host_slots = host_slots;
   p->host_free.resize(host_slots);
   for (int64_t i = 0; i < host_slots; ++i)
@@ -724,10 +757,12 @@ extern "C" kv_status kv_spill(kv_pool* p, int32_t n, const int32_t* ids,
   for (size_t k = 0; k < src.size(); ++k)
     dst.push_back(p->host_free[p->host_free.size() - 1 - k]);
   if (p->has_data() && !src.empty()) {
-    int err = pkv::launch_block_transfer(
-        p->k_pool, p->v_pool, p->num_blocks, p->host_k, p->host_v,
-        p->host_slots, p->num_layers, p->num_kv_heads, p->head_dim, src.data(),
-        dst.data(), (int)src.size(), stream);
+    const pkv::PoolBufs dev{p->k_pool, p->v_pool, p->kv_scales, p->num_blocks};
+    const pkv::PoolBufs host{p->host_k, p->host_v, p->host_scales,
+                             p->host_slots};
+    int err = pkv::launch_block_move(dev, host, p->num_layers, p->tile_bytes(),
+                                     p->scale_bytes(), src.data(), dst.data(),
+                                     (int)src.size(), stream);
     if (err) return fail(KV_ERR_CUDA, "spill copy launch failed (cuda %d)", err);
   }
   // Commit in the same order the slots were taken.
@@ -769,10 +804,12 @@ extern "C" kv_status kv_restore(kv_pool* p, int32_t n, const int32_t* ids,
   for (size_t k = 0; k < src.size(); ++k)
     dst.push_back(p->free_stack[p->free_stack.size() - 1 - k]);
   if (p->has_data() && !src.empty()) {
-    int err = pkv::launch_block_transfer(
-        p->host_k, p->host_v, p->host_slots, p->k_pool, p->v_pool,
-        p->num_blocks, p->num_layers, p->num_kv_heads, p->head_dim, src.data(),
-        dst.data(), (int)src.size(), stream);
+    const pkv::PoolBufs dev{p->k_pool, p->v_pool, p->kv_scales, p->num_blocks};
+    const pkv::PoolBufs host{p->host_k, p->host_v, p->host_scales,
+                             p->host_slots};
+    int err = pkv::launch_block_move(host, dev, p->num_layers, p->tile_bytes(),
+                                     p->scale_bytes(), src.data(), dst.data(),
+                                     (int)src.size(), stream);
     if (err)
       return fail(KV_ERR_CUDA, "restore copy launch failed (cuda %d)", err);
   }

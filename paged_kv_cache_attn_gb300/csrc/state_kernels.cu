@@ -1,18 +1,23 @@
-// Data movement behind kv_append and kv_fork_branches.
+// Data movement behind kv_append, kv_append_batch, kv_fork_branches,
+// kv_spill and kv_restore.
 //
-// Pool layout: [layer][block][kv_head][16 slots][head_dim] bf16, so one
+// bf16 pool layout: [layer][block][kv_head][16 slots][head_dim], so one
 // (block, kv_head) is a contiguous 16 x d tile (4 KB at d = 128) and one
-// token's row of one head is d contiguous values.  Both kernels move 16-byte
-// vectors with grid-stride loops; destinations come from the host allocator
-// and are passed by value (no device-side table).
+// token's row of one head is d contiguous values.  e4m3 pools keep the same
+// tile order with 1-byte codes in the tile layouts of pagedkv.h and a 16-byte
+// scale record per tile.  Copies move 16-byte vectors with grid-stride loops;
+// destinations come from the host allocator and are passed by value (no
+// device-side table).
 
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstdint>
+#include <unordered_map>
 #include <vector>
 
-#include "internal.h"
+#include "device_common.cuh"
+#include "e4m3.cuh"
 
 namespace pkv {
 namespace {
@@ -59,60 +64,45 @@ __global__ void append_scatter_kernel(const __grid_constant__ ScatterArgs a) {
   }
 }
 
-struct CopyArgs {
-  uint4* k_pool;
-  uint4* v_pool;
-  int64_t num_blocks;
+// Whole-block moves (copy-on-write, spill, restore): for pair i, every
+// layer's (block src[i]) bytes of K, V and the scale records of `from` go to
+// block dst[i] of `to`, as 16-byte vectors.
+struct MoveArgs {
+  const uint4* from_k;
+  const uint4* from_v;
+  const uint4* from_s;
+  uint4* to_k;
+  uint4* to_v;
+  uint4* to_s;
+  int64_t from_blocks, to_blocks;
   int L;
-  int vec_per_block;  // Hkv * 16 * d / 8 (one layer)
+  int kv_vecs;  // 16-byte vectors of one (layer, block) in K (and in V)
+  int s_vecs;   // ... in the scale records (0 for bf16 pools)
   int n;
   int src[kMaxDst / 2];
   int dst[kMaxDst / 2];
 };
 
-__global__ void block_copy_kernel(const __grid_constant__ CopyArgs a) {
-  const int64_t per_pair = (int64_t)a.L * a.vec_per_block;
-  const int64_t total = per_pair * a.n;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int pair = (int)(i / per_pair);
-    int64_t r = i - pair * per_pair;
-    const int64_t layer = r / a.vec_per_block;
-    const int64_t vec = r - layer * a.vec_per_block;
-    const int64_t layer_base = layer * a.num_blocks;
-    const int64_t s = (layer_base + a.src[pair]) * a.vec_per_block + vec;
-    const int64_t d = (layer_base + a.dst[pair]) * a.vec_per_block + vec;
-    a.k_pool[d] = a.k_pool[s];
-    a.v_pool[d] = a.v_pool[s];
-  }
-}
-
-struct XferArgs {
-  const uint4* src_k;
-  const uint4* src_v;
-  uint4* dst_k;
-  uint4* dst_v;
-  int64_t src_blocks, dst_blocks;
-  int L;
-  int vec_per_block;  // Hkv * 16 * d / 8 (one layer)
-  int n;
-  int src[kMaxDst / 2];
-  int dst[kMaxDst / 2];
-};
-
-__global__ void block_transfer_kernel(const __grid_constant__ XferArgs a) {
-  const int64_t per_pair = (int64_t)a.L * a.vec_per_block;
+__global__ void block_move_kernel(const __grid_constant__ MoveArgs a) {
+  const int per_layer = 2 * a.kv_vecs + a.s_vecs;
+  const int64_t per_pair = (int64_t)a.L * per_layer;
   const int64_t total = per_pair * a.n;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int pair = (int)(i / per_pair);
     const int64_t r = i - pair * per_pair;
-    const int64_t layer = r / a.vec_per_block;
-    const int64_t vec = r - layer * a.vec_per_block;
-    const int64_t s = (layer * a.src_blocks + a.src[pair]) * a.vec_per_block + vec;
-    const int64_t d = (layer * a.dst_blocks + a.dst[pair]) * a.vec_per_block + vec;
-    a.dst_k[d] = a.src_k[s];
-    a.dst_v[d] = a.src_v[s];
+    const int64_t layer = r / per_layer;
+    int vec = (int)(r - layer * per_layer);
+    const int64_t fb = layer * a.from_blocks + a.src[pair];
+    const int64_t tb = layer * a.to_blocks + a.dst[pair];
+    if (vec < a.kv_vecs) {
+      a.to_k[tb * a.kv_vecs + vec] = a.from_k[fb * a.kv_vecs + vec];
+    } else if ((vec -= a.kv_vecs) < a.kv_vecs) {
+      a.to_v[tb * a.kv_vecs + vec] = a.from_v[fb * a.kv_vecs + vec];
+    } else {
+      vec -= a.kv_vecs;
+      a.to_s[tb * a.s_vecs + vec] = a.from_s[fb * a.s_vecs + vec];
+    }
   }
 }
 
@@ -265,55 +255,201 @@ int launch_append_batch(void* k_pool, void* v_pool, const void* k_new,
   return flush();
 }
 
-int launch_block_transfer(const void* src_k, const void* src_v,
-                          int64_t src_blocks, void* dst_k, void* dst_v,
-                          int64_t dst_blocks, int L, int Hkv, int d,
-                          const int32_t* src, const int32_t* dst, int n,
-                          void* stream) {
-  XferArgs a;
-  a.src_k = static_cast<const uint4*>(src_k);
-  a.src_v = static_cast<const uint4*>(src_v);
-  a.dst_k = static_cast<uint4*>(dst_k);
-  a.dst_v = static_cast<uint4*>(dst_v);
-  a.src_blocks = src_blocks;
-  a.dst_blocks = dst_blocks;
+int launch_block_move(const PoolBufs& from, const PoolBufs& to, int L,
+                      int64_t kv_bytes, int64_t s_bytes, const int32_t* src,
+                      const int32_t* dst, int n, void* stream) {
+  MoveArgs a;
+  a.from_k = static_cast<const uint4*>(from.k);
+  a.from_v = static_cast<const uint4*>(from.v);
+  a.from_s = static_cast<const uint4*>(from.s);
+  a.to_k = static_cast<uint4*>(const_cast<void*>(to.k));
+  a.to_v = static_cast<uint4*>(const_cast<void*>(to.v));
+  a.to_s = static_cast<uint4*>(const_cast<void*>(to.s));
+  a.from_blocks = from.blocks;
+  a.to_blocks = to.blocks;
   a.L = L;
-  a.vec_per_block = Hkv * 16 * d / 8;
+  a.kv_vecs = (int)(kv_bytes / 16);
+  a.s_vecs = (int)(s_bytes / 16);
   for (int i0 = 0; i0 < n; i0 += kMaxDst / 2) {
     a.n = std::min(n - i0, kMaxDst / 2);
     for (int i = 0; i < a.n; ++i) {
       a.src[i] = src[i0 + i];
       a.dst[i] = dst[i0 + i];
     }
-    const int64_t work = (int64_t)a.n * L * a.vec_per_block;
-    block_transfer_kernel<<<grid_for(work), 256, 0, (cudaStream_t)stream>>>(a);
+    const int64_t work = (int64_t)a.n * L * (2 * a.kv_vecs + a.s_vecs);
+    block_move_kernel<<<grid_for(work), 256, 0, (cudaStream_t)stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
   }
   return 0;
 }
 
-int launch_block_copy(void* k_pool, void* v_pool, int64_t num_blocks, int L,
-                      int Hkv, int d, int B, const int32_t* src,
-                      const int32_t* dst, int n, void* stream) {
-  CopyArgs a;
-  a.k_pool = static_cast<uint4*>(k_pool);
-  a.v_pool = static_cast<uint4*>(v_pool);
+// ---- e4m3 pools: quantising writes --------------------------------------------
+
+namespace {
+
+struct E4m3Group {
+  int32_t phys, w0, nw, pad;  // block, its writes [w0, w0 + nw)
+};
+struct E4m3Write {
+  int32_t s0, s1, row, pad;   // slots [s0, s1) <- input rows row ..
+};
+constexpr int kMaxE4m3Groups = 512;
+constexpr int kMaxE4m3Writes = 1024;
+
+struct E4m3AppendArgs {
+  uint8_t* k8;
+  uint8_t* v8;
+  float4* scales;
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  int64_t num_blocks;
+  int L, Hkv, d, total;
+  E4m3Group groups[kMaxE4m3Groups];
+  E4m3Write writes[kMaxE4m3Writes];
+};
+
+// grid (groups, layers, kv-heads); warp 0 writes K, warp 1 writes V.  A
+// block's writes are applied in order by the same warp.
+__global__ void __launch_bounds__(64)
+    append_e4m3_kernel(const __grid_constant__ E4m3AppendArgs a) {
+  const E4m3Group g = a.groups[blockIdx.x];
+  const int layer = blockIdx.y, h = blockIdx.z;
+  const bool is_v = threadIdx.x >= 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t tile = ((int64_t)layer * a.num_blocks + g.phys) * a.Hkv + h;
+  uint8_t* codes = (is_v ? a.v8 : a.k8) + tile * 16 * a.d;
+  float* scale = reinterpret_cast<float*>(a.scales + tile) + (is_v ? 1 : 0);
+  const __nv_bfloat16* src = is_v ? a.v_new : a.k_new;
+  for (int w = g.w0; w < g.w0 + g.nw; ++w) {
+    const E4m3Write wr = a.writes[w];
+    const __nv_bfloat16* rows =
+        src + (((int64_t)layer * a.total + wr.row) * a.Hkv + h) * a.d;
+    e4m3_tile_write(codes, scale, wr.s0, wr.s1, rows, (int64_t)a.Hkv * a.d,
+                    a.d, is_v, lane);
+  }
+}
+
+struct E4m3StepArgs {
+  uint8_t* k8;
+  uint8_t* v8;
+  float4* scales;
+  const __nv_bfloat16* k_step;
+  const __nv_bfloat16* v_step;
+  const int32_t* tables;
+  const int32_t* seq_lens;
+  DeviceStatus* status;
+  int64_t num_blocks;
+  int Hkv, d, max_blocks;
+};
+
+// grid (nb, kv-heads): branch b's newest token into its slot.
+__global__ void __launch_bounds__(64)
+    append_step_e4m3_kernel(const E4m3StepArgs a) {
+  const int b = blockIdx.x, h = blockIdx.y;
+  const bool is_v = threadIdx.x >= 32;
+  const int lane = threadIdx.x & 31;
+  const int t = a.seq_lens[b] - 1;
+  const int lb = t >> 4;
+  const int phys = t >= 0 && lb < a.max_blocks
+                       ? a.tables[(int64_t)b * a.max_blocks + lb] : -1;
+  if (phys < 0 || (int64_t)phys >= a.num_blocks) {
+    if (threadIdx.x == 0) record_status(a.status, KV_ERR_DEVICE, phys);
+    return;
+  }
+  const int64_t tile = (int64_t)phys * a.Hkv + h;
+  uint8_t* codes = (is_v ? a.v8 : a.k8) + tile * 16 * a.d;
+  float* scale = reinterpret_cast<float*>(a.scales + tile) + (is_v ? 1 : 0);
+  const __nv_bfloat16* row =
+      (is_v ? a.v_step : a.k_step) + ((int64_t)b * a.Hkv + h) * a.d;
+  e4m3_tile_write(codes, scale, t & 15, (t & 15) + 1, row, 0, a.d, is_v, lane);
+}
+
+}  // namespace
+
+int launch_append_e4m3(void* k8, void* v8, void* scales, int64_t num_blocks,
+                       int L, int Hkv, int d, const void* k_new,
+                       const void* v_new, int32_t total,
+                       const std::vector<ScatterRun>& runs, void* stream) {
+  // Per-block write lists in program order.
+  std::vector<int32_t> order;                       // distinct blocks
+  std::vector<std::vector<E4m3Write>> per_block;    // parallel to order
+  std::unordered_map<int32_t, int32_t> index;
+  for (const ScatterRun& run : runs) {
+    int tok = 0;
+    while (tok < run.n) {
+      const int t = run.tok0 + tok;
+      const int lb = t / 16;
+      const int s0 = t % 16;
+      const int cnt = std::min(16 - s0, run.n - tok);
+      const int32_t phys = run.dst[lb - run.first_lblock];
+      auto it = index.find(phys);
+      int32_t gi;
+      if (it == index.end()) {
+        gi = (int32_t)order.size();
+        index.emplace(phys, gi);
+        order.push_back(phys);
+        per_block.emplace_back();
+      } else {
+        gi = it->second;
+      }
+      per_block[gi].push_back({s0, s0 + cnt, run.row + tok, 0});
+      tok += cnt;
+    }
+  }
+  E4m3AppendArgs a;
+  a.k8 = static_cast<uint8_t*>(k8);
+  a.v8 = static_cast<uint8_t*>(v8);
+  a.scales = static_cast<float4*>(scales);
+  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
   a.num_blocks = num_blocks;
   a.L = L;
-  a.vec_per_block = Hkv * B * d / 8;
-  for (int i0 = 0; i0 < n; i0 += kMaxDst / 2) {
-    a.n = std::min(n - i0, kMaxDst / 2);
-    for (int i = 0; i < a.n; ++i) {
-      a.src[i] = src[i0 + i];
-      a.dst[i] = dst[i0 + i];
+  a.Hkv = Hkv;
+  a.d = d;
+  a.total = total;
+  size_t gi = 0;
+  while (gi < order.size()) {
+    int ng = 0, nw = 0;
+    while (gi < order.size() && ng < kMaxE4m3Groups) {
+      const auto& ws = per_block[gi];
+      if ((size_t)nw + ws.size() > (size_t)kMaxE4m3Writes) {
+        if (ng > 0) break;
+        return (int)cudaErrorInvalidValue;  // one block written > 1024 times
+      }
+      a.groups[ng] = {order[gi], nw, (int32_t)ws.size(), 0};
+      for (const E4m3Write& w : ws) a.writes[nw++] = w;
+      ++ng;
+      ++gi;
     }
-    const int64_t work = (int64_t)a.n * L * a.vec_per_block;
-    block_copy_kernel<<<grid_for(work), 256, 0, (cudaStream_t)stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    append_e4m3_kernel<<<dim3(ng, L, Hkv), 64, 0, (cudaStream_t)stream>>>(a);
+    const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
   }
   return 0;
+}
+
+int launch_append_step_e4m3(void* k8, void* v8, void* scales,
+                            int64_t num_blocks, int Hkv, int d,
+                            const int32_t* tables, const int32_t* seq_lens,
+                            int nb, int max_blocks, const void* k_step,
+                            const void* v_step, DeviceStatus* status,
+                            void* stream) {
+  E4m3StepArgs a;
+  a.k8 = static_cast<uint8_t*>(k8);
+  a.v8 = static_cast<uint8_t*>(v8);
+  a.scales = static_cast<float4*>(scales);
+  a.k_step = static_cast<const __nv_bfloat16*>(k_step);
+  a.v_step = static_cast<const __nv_bfloat16*>(v_step);
+  a.tables = tables;
+  a.seq_lens = seq_lens;
+  a.status = status;
+  a.num_blocks = num_blocks;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.max_blocks = max_blocks;
+  append_step_e4m3_kernel<<<dim3(nb, Hkv), 64, 0, (cudaStream_t)stream>>>(a);
+  return (int)cudaGetLastError();
 }
 
 }  // namespace pkv

@@ -28,20 +28,48 @@ class Cache:
     """A pool holding one workload's tree, built through the C ABI."""
 
     def __init__(self, w, with_data: bool = True, device: str = "cuda",
-                 evict: bool = True):
+                 evict: bool = True, kv_dtype: str = "bf16",
+                 poison: bool = False, replay: bool = True):
+        """kv_dtype: "bf16" or "e4m3" (codes [L][blocks][Hkv][16 * d] uint8
+        plus scale records [L][blocks][Hkv][4] float32).  poison: fill the
+        pools with NaN (bf16 NaN, e4m3 NaN codes and NaN scales) before any
+        write.  replay=False: create the pool only (no ops, no eviction)."""
         self.w = w
         self.with_data = with_data
         self.device = device
-        self.k = self.v = None
+        self.kv_dtype = kv_dtype
+        self.e4m3 = kv_dtype == "e4m3"
+        if kv_dtype not in ("bf16", "e4m3"):
+            raise ValueError(kv_dtype)
+        self.k = self.v = self.scales = None
         if with_data:
             import torch
-            shape = (w.num_layers, w.num_blocks, w.Hkv, w.block_size, w.d)
-            self.k = torch.empty(shape, dtype=torch.bfloat16, device=device)
-            self.v = torch.empty(shape, dtype=torch.bfloat16, device=device)
-        self.h = B.kv_pool_create(w.num_blocks, w.num_layers, w.Hkv, w.d,
-                                  self.k, self.v, w.initial_free_order(),
-                                  w.block_size)
+            if self.e4m3:
+                shape = (w.num_layers, w.num_blocks, w.Hkv, w.block_size * w.d)
+                self.k = torch.empty(shape, dtype=torch.uint8, device=device)
+                self.v = torch.empty(shape, dtype=torch.uint8, device=device)
+                self.scales = torch.zeros(
+                    (w.num_layers, w.num_blocks, w.Hkv, 4),
+                    dtype=torch.float32, device=device)
+                if poison:
+                    self.k.fill_(0x7F)
+                    self.v.fill_(0x7F)
+                    self.scales.fill_(float("nan"))
+            else:
+                shape = (w.num_layers, w.num_blocks, w.Hkv, w.block_size, w.d)
+                self.k = torch.empty(shape, dtype=torch.bfloat16, device=device)
+                self.v = torch.empty(shape, dtype=torch.bfloat16, device=device)
+                if poison:
+                    self.k.fill_(float("nan"))
+                    self.v.fill_(float("nan"))
+        self.h = B.kv_pool_create(
+            w.num_blocks, w.num_layers, w.Hkv, w.d, self.k, self.v,
+            w.initial_free_order(), w.block_size,
+            B.KV_DTYPE_E4M3 if self.e4m3 else B.KV_DTYPE_BF16, self.scales)
         self.evicted: list = []
+        self.decode_ids: list = []
+        if not replay:
+            return
         self._replay()
         if evict and w.evict_target_leaves() > 0:
             cand = w.evict_candidates()
@@ -113,6 +141,8 @@ class Cache:
             import torch
             num_sms = torch.cuda.get_device_properties(
                 self.device).multi_processor_count
+        if self.e4m3:
+            flags |= B.KV_PLAN_KV_E4M3
         plan, info = B.paged_decode_plan(nb, self.w.Hq, self.w.Hkv, self.w.d,
                                          max_blocks, lens, groups, num_sms,
                                          flags, self.w.block_size)
@@ -156,6 +186,14 @@ class Batch:
         if self.dev is None:
             self.upload()
         d = self.dev
+        if c.e4m3:
+            B.paged_decode_attn_e4m3(
+                q, c.k[layer], c.v[layer], c.scales[layer], w.num_blocks,
+                d["tables"], d["seq_lens"], d["groups"], len(self.groups),
+                self.nb, self.tables.shape[1], w.Hq, w.Hkv, w.d, w.scale, out,
+                d["plan"], self.info, d["workspace"], d["workspace"].numel(),
+                stream, w.block_size)
+            return
         B.paged_decode_attn(q, c.k[layer], c.v[layer], w.num_blocks,
                             d["tables"], d["seq_lens"], d["groups"],
                             len(self.groups), self.nb, self.tables.shape[1],
@@ -172,6 +210,14 @@ class Batch:
         if self.dev is None:
             self.upload()
         d = self.dev
+        if c.e4m3:
+            B.paged_decode_append_attn_e4m3(
+                q, k_step, v_step, c.k[layer], c.v[layer], c.scales[layer],
+                w.num_blocks, d["tables"], d["seq_lens"], d["groups"],
+                len(self.groups), self.nb, self.tables.shape[1], w.Hq, w.Hkv,
+                w.d, w.scale, out, d["plan"], self.info, d["workspace"],
+                d["workspace"].numel(), stream, w.block_size)
+            return
         B.paged_decode_append_attn(q, k_step, v_step, c.k[layer], c.v[layer],
                                    w.num_blocks, d["tables"], d["seq_lens"],
                                    d["groups"], len(self.groups), self.nb,

@@ -110,17 +110,7 @@ def test_pool_bytes_bit_exact(built, name):
 def test_poisoned_free_slots_do_not_leak(built):
     """Slots past a branch's length hold NaN: the output must not see them."""
     w = SMALL["long_context"]()
-    cache = H.Cache.__new__(H.Cache)
-    # Build with NaN-filled pools: allocate, poison, then replay.
-    cache.w, cache.with_data, cache.device = w, True, "cuda"
-    shape = (w.num_layers, w.num_blocks, w.Hkv, w.block_size, w.d)
-    cache.k = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
-    cache.v = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
-    cache.h = B.kv_pool_create(w.num_blocks, w.num_layers, w.Hkv, w.d, cache.k,
-                               cache.v, w.initial_free_order())
-    cache.evicted = []
-    cache._replay()
-    cache.decode_ids = w.leaves()
+    cache = H.Cache(w, poison=True)
     ref = rp.replay(w, with_data=True)
     q = w.queries(len(cache.decode_ids))
     gpu, _ = run_decode(cache, q)
@@ -190,13 +180,7 @@ def test_batched_append_pool_bytes(built):
     """Children's first segments appended in one kv_append_batch land where
     the oracle's sequential appends put them."""
     w = SMALL["fanout"]()
-    cache = H.Cache.__new__(H.Cache)
-    cache.w, cache.with_data, cache.device = w, True, "cuda"
-    shape = (w.num_layers, w.num_blocks, w.Hkv, w.block_size, w.d)
-    cache.k = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
-    cache.v = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
-    cache.h = B.kv_pool_create(w.num_blocks, w.num_layers, w.Hkv, w.d, cache.k,
-                               cache.v, w.initial_free_order())
+    cache = H.Cache(w, replay=False)
     pending = []                        # consecutive appends -> one batch
 
     def flush():

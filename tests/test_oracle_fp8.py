@@ -238,3 +238,25 @@ def test_decode_step_fp8_equals_attention_on_dequantised_values():
     ref = brute.single_query(att.bf16_to_f64(q[b, h]).tolist(), K.tolist(),
                              V.tolist(), w.scale)
     assert np.allclose(out[b, h], ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("name", ["tiny_tree", "deep_tree"])
+def test_sequence_route_equals_pool_route(name):
+    """Quantising a branch from its logical token sequence and its append
+    history gives, bit for bit, the values the replayed pool holds for it
+    (through forks with copy-on-write and multi-block appends)."""
+    w = (wl.make("tiny_tree") if name == "tiny_tree"
+         else wl.deep_tree(root_tokens=300, depth=3, min_seg=5, max_seg=40))
+    r8 = rp.replay(w, with_data=True, kv_dtype="e4m3")
+    kf, vf = r8.data.values(0)
+    for nid in r8.decode_ids:
+        node = r8.model.nodes[nid]
+        kb, vb = r8.branch_kv(nid)
+        lens = [hi - lo for _src, lo, hi in r8.logical[nid]]
+        kq = fp8.quantize_sequence(lens, kb)
+        vq = fp8.quantize_sequence(lens, vb)
+        for g in range(w.Hkv):
+            K = fp8.gather_values(kf, node.table, node.seq_len, g, 16)
+            V = fp8.gather_values(vf, node.table, node.seq_len, g, 16)
+            assert np.array_equal(K, kq[0, :, g])
+            assert np.array_equal(V, vq[0, :, g])
