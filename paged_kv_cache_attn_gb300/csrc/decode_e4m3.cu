@@ -19,10 +19,14 @@
 //    4q .. 4q + 3, which is the A operand of O += P V, and the V tile's
 //    16-byte unit (dimension group, token group q) holds exactly those four
 //    tokens for four dimensions: one load gives four n-tiles' B operands.
+//  * Each warp takes two of its blocks per iteration: four independent QK
+//    accumulation chains, one softmax update over 32 tokens.  The softmax
+//    keeps a lazy reference maximum per row that moves (rescaling O and l)
+//    only when a block raises the row maximum by more than 2^8.
 //  * Codes widen to f16 exactly (cvt e4m3x2 -> f16x2).  The K scale folds
 //    into the per-row score multiplier; the V scale folds into P relative to
 //    a running power-of-two reference (O is rescaled when a larger V scale
-//    arrives), so P stays in [0, 1] in f16.  q is scaled per row by a power
+//    arrives), so P stays below 2^8 in f16.  q is scaled per row by a power
 //    of two so its largest element lies in [2^14, 2^15) before the f16
 //    conversion, and the factor is folded back into the scores.
 //  * Masked slots may hold any code (NaN included): their scores are -inf
@@ -227,108 +231,184 @@ __global__ void __launch_bounds__(128, 2)
 
   bool timed_out = false;
   int k = 0;
-  for (; k < my_n; ++k) {
-    const int s = k % NS;
-    const uint32_t st = ring + s * C::kStage;
-    if (!mbar_wait(bar0 + s * 8, (k / NS) & 1)) {
-      timed_out = true;
-      break;
-    }
-    const int j = it.blk_begin + warp + C::kWarps * k;
-    if (!((bad >> s) & 1)) {
-      int nv = seq_len - j * 16;
-      nv = nv > 16 ? 16 : nv;
-      const uint32_t kt = st, vt = st + C::kTile;
-      const float2 scl = lds64f(st + 2 * C::kTile);  // (K scale, V scale)
-
-      // S = Q K^T for the block's 16 tokens.
-      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  // Two of the warp's blocks per iteration (a and a + 1 of its sequence):
+  // four independent QK accumulation chains and one softmax update over 32
+  // tokens.  m_r is a lazy reference maximum: it moves (and O, l are
+  // rescaled) only when a row's maximum exceeds it by more than 2^8, so the
+  // weights 2^(x - m_r) stay below 2^8 and f16 P keeps them.
+  for (; k < my_n; k += 2) {
+    const int nblk2 = k + 1 < my_n ? 2 : 1;
+    int stg[2], nv[2];
+    bool use[2];
+    float2 scl[2];
 #pragma unroll
-      for (int jn = 0; jn < 2; ++jn) {
-        const int tk = 4 * (gq >> 1) + 2 * jn + (gq & 1);
-#pragma unroll
-        for (int kq = 0; kq < C::kChunks; ++kq) {
-          const int c = D == 128 ? 2 * tq + kq : tq;
-          const int pc = D == 128 ? (c ^ (tk & 7)) : c;
-          const uint4 w = lds128(kt + tk * D + pc * 16);
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            mma_16816_f16(sacc[jn], qa[4 * kq + i], e4m3x2_to_f16x2(ws[i]),
-                          e4m3x2_to_f16x2(ws[i] >> 16));
-        }
+    for (int u = 0; u < 2; ++u) {
+      stg[u] = (k + u) % NS;
+      use[u] = false;
+      nv[u] = 0;
+      scl[u] = make_float2(0.f, 0.f);
+      if (u < nblk2) {
+        if (!mbar_wait(bar0 + stg[u] * 8, ((k + u) / NS) & 1)) timed_out = true;
+        use[u] = !((bad >> stg[u]) & 1);
+        const int j = it.blk_begin + warp + C::kWarps * (k + u);
+        const int n = seq_len - j * 16;
+        nv[u] = use[u] ? (n > 16 ? 16 : n) : 0;
+        if (use[u]) scl[u] = lds64f(ring + stg[u] * C::kStage + 2 * C::kTile);
       }
-      // Scale, mask, online softmax (base 2).
-      float x[2][4];
+    }
+    if (timed_out) break;
+
+    // S = Q K^T for both blocks.
+    float sacc[2][2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
 #pragma unroll
       for (int jn = 0; jn < 2; ++jn)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int tok = 4 * tq + 2 * jn + (i & 1);
-          x[jn][i] = tok < nv ? sacc[jn][i] * (fsc[i >> 1] * scl.x) : -INFINITY;
+        for (int i = 0; i < 4; ++i) sacc[u][jn][i] = 0.f;
+#pragma unroll
+    for (int kq = 0; kq < C::kChunks; ++kq) {
+      uint4 w[2][2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int jn = 0; jn < 2; ++jn) {
+          const int tk = 4 * (gq >> 1) + 2 * jn + (gq & 1);
+          const int c = D == 128 ? 2 * tq + kq : tq;
+          const int pc = D == 128 ? (c ^ (tk & 7)) : c;
+          w[u][jn] = use[u] ? lds128(ring + stg[u] * C::kStage + tk * D + pc * 16)
+                            : make_uint4(0, 0, 0, 0);
         }
-      // A larger V scale than the reference: rescale O to it.
-      float vfac = 1.f;
-      if (scl.y > vref) {
-        vfac = vref / scl.y;
-        vref = scl.y;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int jn = 0; jn < 2; ++jn) {
+            const uint32_t wd = i == 0   ? w[u][jn].x
+                                : i == 1 ? w[u][jn].y
+                                : i == 2 ? w[u][jn].z
+                                         : w[u][jn].w;
+            uint32_t b0, b1;
+            e4m3x4_to_f16x2x2(wd, b0, b1);
+            mma_16816_f16(sacc[u][jn], qa[4 * kq + i], b0, b1);
+          }
+    }
+    // Scale, mask (tokens past nv, and blocks not in use).
+    float x[2][2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const float f0 = fsc[0] * scl[u].x, f1 = fsc[1] * scl[u].x;
+#pragma unroll
+      for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          x[u][jn][i] = sacc[u][jn][i] * (i < 2 ? f0 : f1);
+      if (nv[u] < 16) {
+#pragma unroll
+        for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (4 * tq + 2 * jn + (i & 1) >= nv[u]) x[u][jn][i] = -INFINITY;
       }
-      const float pfac = scl.y / vref;
+    }
+    // V scale reference: the largest V scale seen so far.
+    const float vmax = fmaxf(scl[0].y, scl[1].y);
+    float vfac = 1.f;
+    if (vmax > vref) {
+      vfac = vref / vmax;
+      vref = vmax;
+    }
+    float alpha[2];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+        mx = fmaxf(mx, fmaxf(fmaxf(x[u][0][2 * hr], x[u][0][2 * hr + 1]),
+                             fmaxf(x[u][1][2 * hr], x[u][1][2 * hr + 1])));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      alpha[hr] = 1.f;
+      if (mx > m_r[hr] + 8.f) {  // also when m_r is -inf and mx finite
+        alpha[hr] = ex2(m_r[hr] - mx);
+        m_r[hr] = mx;
+      }
+    }
+    if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f) ||
+        vfac != 1.f) {
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        l_r[hr] *= alpha[hr];
+        const float f = alpha[hr] * vfac;
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) {
+          o[nt][2 * hr] *= f;
+          o[nt][2 * hr + 1] *= f;
+        }
+      }
+    }
+    uint32_t pa[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const float pfac = use[u] ? scl[u].y / vref : 0.f;
       float pr[2][4];
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
-        float mx = fmaxf(fmaxf(x[0][2 * hr], x[0][2 * hr + 1]),
-                         fmaxf(x[1][2 * hr], x[1][2 * hr + 1]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_r[hr], mx);
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = ex2(m_r[hr] - m_use);
-        m_r[hr] = m_new;
+        const float m_use = m_r[hr] == -INFINITY ? 0.f : m_r[hr];
         float sum = 0.f;
 #pragma unroll
         for (int jn = 0; jn < 2; ++jn)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const float pv = ex2(x[jn][2 * hr + e] - m_use);
+            const float pv = ex2(x[u][jn][2 * hr + e] - m_use);
             pr[jn][2 * hr + e] = pv * pfac;
             sum += pv;
           }
-        l_r[hr] = l_r[hr] * alpha + sum;
-        const float ofac = alpha * vfac;
-#pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt) {
-          o[nt][2 * hr] *= ofac;
-          o[nt][2 * hr + 1] *= ofac;
-        }
+        l_r[hr] += sum;
       }
-      uint32_t pa[4];
-      pa[0] = pack_f16(pr[0][0], pr[0][1]);
-      pa[1] = pack_f16(pr[0][2], pr[0][3]);
-      pa[2] = pack_f16(pr[1][0], pr[1][1]);
-      pa[3] = pack_f16(pr[1][2], pr[1][3]);
-      // Bytes of tokens at or past nv are zeroed before widening.
-      int keep = nv - 4 * tq;
+      pa[u][0] = pack_f16(pr[0][0], pr[0][1]);
+      pa[u][1] = pack_f16(pr[0][2], pr[0][3]);
+      pa[u][2] = pack_f16(pr[1][0], pr[1][1]);
+      pa[u][3] = pack_f16(pr[1][2], pr[1][3]);
+    }
+    // O += P V for each block in use; bytes of tokens at or past nv are
+    // zeroed before widening (masked slots may hold NaN codes).
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (!use[u]) continue;
+      int keep = nv[u] - 4 * tq;
       keep = keep < 0 ? 0 : (keep > 4 ? 4 : keep);
       const uint32_t vmask = keep == 4 ? 0xffffffffu : ((1u << (8 * keep)) - 1u);
-      // O += P V: unit (dimension group 8p + gq, token group tq).
+      const uint32_t vt = ring + stg[u] * C::kStage + C::kTile;
 #pragma unroll
       for (int pp = 0; pp < D / 32; ++pp) {
-        const uint4 w = lds128(vt + ((8 * pp + gq) * 4 + tq) * 16);
-        const uint32_t ws[4] = {w.x & vmask, w.y & vmask, w.z & vmask,
-                                w.w & vmask};
+        uint4 w = lds128(vt + ((8 * pp + gq) * 4 + tq) * 16);
+        if (nv[u] < 16) {
+          w.x &= vmask;
+          w.y &= vmask;
+          w.z &= vmask;
+          w.w &= vmask;
+        }
+        uint32_t b[8];
+        e4m3x4_to_f16x2x2(w.x, b[0], b[1]);
+        e4m3x4_to_f16x2x2(w.y, b[2], b[3]);
+        e4m3x4_to_f16x2x2(w.z, b[4], b[5]);
+        e4m3x4_to_f16x2x2(w.w, b[6], b[7]);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          mma_16816_f16(o[4 * pp + i], pa, e4m3x2_to_f16x2(ws[i]),
-                        e4m3x2_to_f16x2(ws[i] >> 16));
+          mma_16816_f16(o[4 * pp + i], pa[u], b[2 * i], b[2 * i + 1]);
       }
     }
     __syncwarp();
-    if (k + NS < my_n) {
-      if (issue(k + NS))
-        bad &= ~(1u << s);
-      else
-        bad |= 1u << s;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (u < nblk2 && k + u + NS < my_n) {
+        if (issue(k + u + NS))
+          bad &= ~(1u << stg[u]);
+        else
+          bad |= 1u << stg[u];
+      }
     }
   }
   if (timed_out) {

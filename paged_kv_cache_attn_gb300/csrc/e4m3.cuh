@@ -53,11 +53,16 @@ __device__ __forceinline__ float e4m3_decode(uint8_t c) {
   return __half2float(__half(h));
 }
 
-// Two codes (low byte first) -> f16x2 (low half = low byte), exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  const __half2_raw h =
-      __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Four codes (bytes 0..3 of w) -> two f16x2, exactly: lo = (byte 0, byte 1),
+// hi = (byte 2, byte 3), the lower byte in the lower half.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo,
+                                                  uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 // Byte offset of (slot t, dimension c) inside a K tile / a V tile.
