@@ -99,8 +99,8 @@ typedef struct kv_pool_desc {
    * slot t, dimension c (0 <= c < head_dim):
    *   K: t * head_dim + c, except that for head_dim 128 the 16-byte chunk
    *      c / 16 of row t sits at chunk position (c / 16) ^ (t % 8);
-   *   V: ((c / 4) * 4 + t / 4) * 16 + (c % 4) * 4 + t % 4 (16-byte units of
-   *      4 dimensions x 4 tokens, dimension-major inside a unit).
+   *   V: c * 16 + t (transposed: one 16-byte row of the 16 slots per
+   *      dimension).
    * Writes quantise on the device: a write that starts a block (slot 0)
    * takes the scale of its own rows; a later write keeps the block's scale
    * unless its rows need a larger one, in which case the rows already

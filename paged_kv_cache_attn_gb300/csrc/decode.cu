@@ -491,6 +491,11 @@ cudaError_t launch_split_e4m3(const SplitParams& sp, const void* k8,
                               const void* v8, const void* scales, int n_items,
                               int d, cudaStream_t stream);
 
+// Tensor-core tile kernel over an e4m3 pool; defined in decode_tc_e4m3.cu.
+cudaError_t launch_tile_e4m3(const SplitParams& sp, const WorkItem* items,
+                             int n_items, const void* k8, const void* v8,
+                             const void* scales, cudaStream_t stream);
+
 // Tensor-core (tcgen05) kernel for 128-row tiles; defined in decode_tc.cu.
 cudaError_t launch_tile_items(const CUtensorMap& tk, const CUtensorMap& tv,
                               const SplitParams& sp, const WorkItem* items,
@@ -590,8 +595,8 @@ static kv_status decode_impl(
     return fail(KV_ERR_INVALID_ARG, e4m3 ? "an e4m3 step needs a plan made "
                                            "with KV_PLAN_KV_E4M3"
                                          : "plan was made for an e4m3 pool");
-  if (e4m3 && info->n_tile_items != 0)
-    return fail(KV_ERR_INVALID_ARG, "e4m3 plan with tensor-core tiles");
+  if (e4m3 && info->n_tile_items != 0 && (d != 128 || info->tile_cluster != 1))
+    return fail(KV_ERR_INVALID_ARG, "e4m3 tiles need head_dim 128, no clusters");
   if ((uintptr_t)workspace & 255)
     return fail(KV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   if (!std::isfinite(scale) || !(scale > 0.f))
@@ -663,9 +668,11 @@ static kv_status decode_impl(
   if (info->n_tile_items > 0) {
     cudaStream_t ts = fork ? side->stream : st;
     pkv::mark(0, ts);
-    e = pkv::launch_tile_items(
-        tk, tv, sp, reinterpret_cast<const pkv::WorkItem*>(plan + off_tile),
-        info->n_tile_items, d, info->tile_cluster, ts);
+    const auto* titems = reinterpret_cast<const pkv::WorkItem*>(plan + off_tile);
+    e = e4m3 ? pkv::launch_tile_e4m3(sp, titems, info->n_tile_items, k_pool,
+                                     v_pool, kv_scales, ts)
+             : pkv::launch_tile_items(tk, tv, sp, titems, info->n_tile_items, d,
+                                      info->tile_cluster, ts);
     pkv::mark(1, ts);
     if (e != cudaSuccess)
       return fail(KV_ERR_CUDA, "tile kernel: %s", cudaGetErrorString(e));

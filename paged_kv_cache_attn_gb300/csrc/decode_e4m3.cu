@@ -16,9 +16,10 @@
 //    XOR chunk swizzle (head_dim 128) makes the eight rows of a load phase
 //    hit eight different bank groups.
 //  * With that token order, a lane's S accumulator columns are tokens
-//    4q .. 4q + 3, which is the A operand of O += P V, and the V tile's
-//    16-byte unit (dimension group, token group q) holds exactly those four
-//    tokens for four dimensions: one load gives four n-tiles' B operands.
+//    4q .. 4q + 3, which is the A operand of O += P V; the V tile is stored
+//    transposed (16 slots per dimension), so those four tokens of the lane's
+//    dimension are one aligned 32-bit word: one load per n-tile, and the 32
+//    lanes of a load read 128 contiguous bytes.
 //  * Each warp takes two of its blocks per iteration: four independent QK
 //    accumulation chains, one softmax update over 32 tokens.  The softmax
 //    keeps a lazy reference maximum per row that moves (rescaling O and l)
@@ -49,32 +50,6 @@ __device__ __forceinline__ void mma_16816_f16(float (&c)[4],
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// 1-D bulk copy global -> shared, completing on `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src,
-                                          uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
-      "[%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
-
-__device__ __forceinline__ float2 lds64f(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];"
-               : "=f"(v.x), "=f"(v.y)
-               : "r"(addr));
-  return v;
 }
 
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
@@ -380,24 +355,16 @@ __global__ void __launch_bounds__(128, 2)
       int keep = nv[u] - 4 * tq;
       keep = keep < 0 ? 0 : (keep > 4 ? 4 : keep);
       const uint32_t vmask = keep == 4 ? 0xffffffffu : ((1u << (8 * keep)) - 1u);
-      const uint32_t vt = ring + stg[u] * C::kStage + C::kTile;
+      const uint32_t vt =
+          ring + stg[u] * C::kStage + C::kTile + gq * 16 + tq * 4;
+      const bool partial = nv[u] < 16;
 #pragma unroll
-      for (int pp = 0; pp < D / 32; ++pp) {
-        uint4 w = lds128(vt + ((8 * pp + gq) * 4 + tq) * 16);
-        if (nv[u] < 16) {
-          w.x &= vmask;
-          w.y &= vmask;
-          w.z &= vmask;
-          w.w &= vmask;
-        }
-        uint32_t b[8];
-        e4m3x4_to_f16x2x2(w.x, b[0], b[1]);
-        e4m3x4_to_f16x2x2(w.y, b[2], b[3]);
-        e4m3x4_to_f16x2x2(w.z, b[4], b[5]);
-        e4m3x4_to_f16x2x2(w.w, b[6], b[7]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          mma_16816_f16(o[4 * pp + i], pa[u], b[2 * i], b[2 * i + 1]);
+      for (int nt = 0; nt < D / 8; ++nt) {
+        uint32_t w = lds32(vt + nt * 128);  // dimension 8 nt + gq
+        if (partial) w &= vmask;
+        uint32_t b0, b1;
+        e4m3x4_to_f16x2x2(w, b0, b1);
+        mma_16816_f16(o[nt], pa[u], b0, b1);
       }
     }
     __syncwarp();
@@ -424,17 +391,16 @@ __global__ void __launch_bounds__(128, 2)
   }
 
   // Combine the four warps' partial states through shared memory; O goes
-  // back to plain units (x vref) and to natural dimension order: n-tile nt,
-  // column n is dimension 32 (nt / 4) + 4 n + nt % 4.
+  // back to plain units (x vref).
   __syncthreads();
   float* Ow = base_ptr + warp * 16 * D;
 #pragma unroll
   for (int nt = 0; nt < D / 8; ++nt) {
-    const int d0 = 32 * (nt >> 2) + 8 * tq + (nt & 3);
-    Ow[gq * D + d0] = o[nt][0] * vref;
-    Ow[gq * D + d0 + 4] = o[nt][1] * vref;
-    Ow[(gq + 8) * D + d0] = o[nt][2] * vref;
-    Ow[(gq + 8) * D + d0 + 4] = o[nt][3] * vref;
+    const int col = nt * 8 + 2 * tq;
+    *reinterpret_cast<float2*>(Ow + gq * D + col) =
+        make_float2(o[nt][0] * vref, o[nt][1] * vref);
+    *reinterpret_cast<float2*>(Ow + (gq + 8) * D + col) =
+        make_float2(o[nt][2] * vref, o[nt][3] * vref);
   }
   if (tq == 0) {
     m_sh[warp][gq] = m_r[0];

@@ -70,9 +70,7 @@ __device__ __forceinline__ int k_tile_offset(int t, int c, int d) {
   if (d == 128) return t * 128 + ((((c >> 4) ^ (t & 7))) << 4) + (c & 15);
   return t * d + c;
 }
-__device__ __forceinline__ int v_tile_offset(int t, int c) {
-  return (((c >> 2) << 2) + (t >> 2)) * 16 + ((c & 3) << 2) + (t & 3);
-}
+__device__ __forceinline__ int v_tile_offset(int t, int c) { return c * 16 + t; }
 
 // Warp-wide: write rows[0 .. s1 - s0) (bf16, row r at rows + r * row_stride,
 // d values) into slots [s0, s1) of one e4m3 tile `codes` whose scale is

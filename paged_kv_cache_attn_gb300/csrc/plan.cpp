@@ -80,11 +80,9 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   if (flags & ~(KV_PLAN_NO_TENSOR_CORES | KV_PLAN_IGNORE_GROUPS |
                 KV_PLAN_KV_E4M3))
     return fail(KV_ERR_INVALID_ARG, "unknown plan flags 0x%x", flags);
-  // The tcgen05 tile kernel is built for bf16 pools with head_dim 128; e4m3
-  // steps run every unit through the split-KV kernel.
+  // The tcgen05 tile kernels are built for head_dim 128 (bf16 and e4m3).
   const bool allow_tc = pkv::kTensorCoreKernel && d == 128 &&
-                        !(flags & KV_PLAN_NO_TENSOR_CORES) &&
-                        !(flags & KV_PLAN_KV_E4M3);
+                        !(flags & KV_PLAN_NO_TENSOR_CORES);
   if (use_groups && n_groups > 0) {
     std::vector<std::vector<std::pair<int32_t, int32_t>>> per_row(nb);
     for (int32_t i = 0; i < n_groups; ++i) {
@@ -138,9 +136,11 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   // Tile units with more than one 128-row tile run as clusters of two CTAs
   // (one per tile of the same segment, kv-head and block range) that share
   // every K/V load; an odd last tile is paired with a row-less partner.
+  // (The e4m3 tile kernel runs single CTAs.)
   int32_t tile_cluster = 1;
   for (const Unit& u : units)
-    if (u.tile && u.rows > pkv::kTileRows) tile_cluster = 2;
+    if (u.tile && u.rows > pkv::kTileRows && !(flags & KV_PLAN_KV_E4M3))
+      tile_cluster = 2;
 
   std::vector<pkv::WorkItem> row_items, tile_items;
   struct Tagged { int32_t branch; pkv::MergeEntry e; };

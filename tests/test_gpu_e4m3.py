@@ -39,6 +39,9 @@ SMALL = {
     "long_context": lambda: W.long_context(n_indep=3, indep_tokens=1000,
                                            n_roots=2, root_tokens=2048,
                                            fan=16, suffix_tokens=37),
+    "fanout_3tiles": lambda: W.fanout(n_roots=1, root_tokens=512, fan=40,
+                                      min_suffix=1, max_suffix=50, Hq=64,
+                                      Hkv=8),
     "gqa_2": lambda: W.independent(n_seqs=3, min_len=17, max_len=300, Hq=8,
                                    Hkv=4, d=64),
     "gqa_16": lambda: W.fanout(n_roots=1, root_tokens=64, fan=3,
@@ -59,7 +62,7 @@ def k_offsets(d):
 def v_offsets(d):
     t = np.arange(16)[:, None]
     c = np.arange(d)[None, :]
-    return ((c >> 2) * 4 + (t >> 2)) * 16 + (c & 3) * 4 + (t & 3)
+    return c * 16 + t
 
 
 def logical_codes(raw, d, kind):
@@ -140,15 +143,21 @@ def test_e4m3_pool_bit_exact(name):
 
 
 @pytest.mark.parametrize("name", list(SMALL))
-@pytest.mark.parametrize("flags", [0, B.KV_PLAN_IGNORE_GROUPS])
+@pytest.mark.parametrize("flags", [0, B.KV_PLAN_IGNORE_GROUPS,
+                                   B.KV_PLAN_NO_TENSOR_CORES])
 def test_e4m3_decode_matches_oracle(name, flags):
+    """Segments of more than 64 rows (head_dim 128) run on the tcgen05 e4m3
+    tile kernel unless the plan says otherwise; the rest on the split-KV
+    kernel."""
     w = SMALL[name]()
     cache = H.Cache(w, kv_dtype="e4m3")
     ref = rp.replay(w, with_data=True, kv_dtype="e4m3")
     assert cache.decode_ids == ref.decode_ids
     q = w.queries(len(cache.decode_ids))
     gpu, bt = run_decode(cache, q, flags)
-    assert bt.info.n_tile_items == 0 and bt.info.flags & B.KV_PLAN_KV_E4M3
+    assert bt.info.flags & B.KV_PLAN_KV_E4M3 and bt.info.tile_cluster == 1
+    if flags or w.d != 128:
+        assert bt.info.n_tile_items == 0
     assert_close(gpu, rp.decode_all_from_pool(ref, q, w.scale), name)
     cache.close()
 
