@@ -7,7 +7,7 @@
 // fragments, conflict-free, with no transpose:
 //  * Tiles arrive with three 1-D bulk copies per block (K codes, V codes, the
 //    16-byte scale record), completing on the stage's mbarrier; each of the
-//    4 warps runs its own 6-stage ring (two CTAs per SM).
+//    4 warps runs its own 4-stage ring (three CTAs per SM).
 //  * S = Q K^T with mma.sync m16n8k16 in f16: lane (n = lane / 4, q = lane %
 //    4) of n-tile j reads token 4(n / 2) + 2j + n % 2 and the head-dimension
 //    slice [q d / 4, (q + 1) d / 4); k-step s of that lane uses dimensions
@@ -68,10 +68,10 @@ struct E4m3Cfg {
   static constexpr int kChunks = D / 64;        // K chunks per lane and row
 };
 
-constexpr int kE4m3Stages = 6;
+constexpr int kE4m3Stages = 4;
 
 template <int D, int NS>
-__global__ void __launch_bounds__(128, 2)
+__global__ void __launch_bounds__(128, 3)
     splitkv_e4m3_kernel(const SplitParams p, const uint8_t* __restrict__ k8,
                         const uint8_t* __restrict__ v8,
                         const float4* __restrict__ scales) {

@@ -438,31 +438,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         vref = vmax;
       }
       const uint32_t srow = lane_base + b * kT;
-      // Pass 1: row maximum over the valid tokens.
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // Pass 1: row maximum over the valid tokens.  The K scale factor of a
+      // block is positive, so the maximum of the scaled scores of a block is
+      // the factor times the maximum of its raw scores.
+      float mx = -INFINITY;
 #pragma unroll 1
       for (int c = 0; c < kT / 32; ++c) {
         uint32_t sv[32];
         tmem_ld32(srow + c * 32, sv);
         tmem_wait_ld();
-        const float f0 = kf[2 * c], f1 = kf[2 * c + 1];
+        float bm[2] = {-INFINITY, -INFINITY};
+        if (valid >= (c + 1) * 32) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (c * 32 + i < valid)
-            mx4[i & 3] = fmaxf(mx4[i & 3],
-                               __uint_as_float(sv[i]) * (i < 16 ? f0 : f1));
+          for (int i = 0; i < 32; ++i)
+            bm[i >> 4] = fmaxf(bm[i >> 4], __uint_as_float(sv[i]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i < valid)
+              bm[i >> 4] = fmaxf(bm[i >> 4], __uint_as_float(sv[i]));
+        }
+        mx = fmaxf(mx, fmaxf(bm[0] * kf[2 * c], bm[1] * kf[2 * c + 1]));
       }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const bool need = mx > m_used + kRescale;
       const float m_new = need ? mx : m_used;
       const float alpha = need ? ex2(m_used - m_new) : 1.f;
       l *= alpha;
       m_used = m_new;
-      // Pass 2: P = 2^(x - m) (V scale relative to vref folded in) as f16.
-      const float neg_m = -m_used;
-      float vr[kTB];
+      // Pass 2: P' = 2^(x - m + log2(vs / vref)) as f16 -- the V scale of the
+      // block relative to vref (a power of two, at most 1) folded into the
+      // exponent -- and l += P' * (vref / vs) per block.  Blocks whose V scale
+      // is below 2^-64 of vref keep the factor 2^-64 (their V values are
+      // negligible next to the largest; l stays exact).
+      float lv[kTB], il[kTB];
 #pragma unroll
-      for (int bb = 0; bb < kTB; ++bb) vr[bb] = vsc[bb] / vref;
+      for (int bb = 0; bb < kTB; ++bb) {
+        const int e = bb < nvb ? scale_exponent(vsc[bb]) - scale_exponent(vref)
+                               : 0;
+        const int ec = e < -64 ? -64 : e;
+        lv[bb] = (float)ec - m_used;
+        il[bb] = pow2f(-ec);
+      }
       uint32_t pk[kT / 2];
 #pragma unroll
       for (int c = 0; c < kT / 32; ++c) {
@@ -470,20 +486,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(srow + c * 32, sv);
         tmem_wait_ld();
         const float f0 = kf[2 * c], f1 = kf[2 * c + 1];
-        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        const float a0 = lv[2 * c], a1 = lv[2 * c + 1];
+        float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        if (valid >= (c + 1) * 32) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int t0 = c * 32 + 2 * i;
-          const float f = i < 8 ? f0 : f1;
-          const float v = i < 8 ? vr[2 * c] : vr[2 * c + 1];
-          float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), f, neg_m));
-          float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), f, neg_m));
-          p0 = t0 < valid ? p0 : 0.f;
-          p1 = t0 + 1 < valid ? p1 : 0.f;
-          acc4[i & 3] += p0 + p1;
-          pk[c * 16 + i] = pack_f16(p0 * v, p1 * v);
+          for (int i = 0; i < 16; ++i) {
+            const bool lo = i < 8;
+            const float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), lo ? f0 : f1,
+                                      lo ? a0 : a1));
+            const float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]),
+                                      lo ? f0 : f1, lo ? a0 : a1));
+            acc[i >> 3][i & 1] += p0 + p1;
+            pk[c * 16 + i] = pack_f16(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const bool lo = i < 8;
+            const int t0 = c * 32 + 2 * i;
+            float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), lo ? f0 : f1,
+                                lo ? a0 : a1));
+            float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), lo ? f0 : f1,
+                                lo ? a0 : a1));
+            p0 = t0 < valid ? p0 : 0.f;
+            p1 = t0 + 1 < valid ? p1 : 0.f;
+            acc[i >> 3][i & 1] += p0 + p1;
+            pk[c * 16 + i] = pack_f16(p0, p1);
+          }
         }
-        l += (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+        l = fmaf(acc[0][0] + acc[0][1], il[2 * c],
+                 fmaf(acc[1][0] + acc[1][1], il[2 * c + 1], l));
       }
       if (j > 0 && !mbar_wait(smem_u32(&bars.pv_done), (j - 1) & 1)) {
         ok = false;
