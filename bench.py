@@ -665,6 +665,9 @@ def run_ours(args):
             win8 = k8ms["tile_e4m3" if has_t else "splitkv_e4m3"]
             kname8 = "tile_e4m3_kernel" if has_t else "splitkv_e4m3_kernel"
         ach8 = alg8 / (win8 / 1e3) / 1e9
+        tr8 = [traffic_per_launch(n, w.name) for n, on in
+               (("tile_e4m3_kernel", has_t), ("splitkv_e4m3_kernel", has_r)) if on]
+        traffic8 = sum(tr8) if tr8 and None not in tr8 else None
         e4m3 = {
             "ms_per_step": round(ms8, 5),
             "unique_kv_bytes": uniq8,
@@ -678,6 +681,7 @@ def run_ours(args):
                 "achieved": round(ach8, 1), "peak": peak,
                 "peak_kind": peak_kind, "unit": "GB/s",
                 "frac": round(ach8 / peak, 4),
+                "traffic": traffic8,
                 "algorithmic_bytes_per_launch": alg8,
                 "ms_per_launch": round(win8, 5),
                 "note": "e4m3 codes + 16-byte scale record per block read; "
