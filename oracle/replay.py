@@ -104,15 +104,16 @@ def decode_rows(r: Replayed, q: np.ndarray, rows, scale: float) -> dict:
     return out
 
 
-def decode_all_from_pool(r: Replayed, q: np.ndarray, scale: float) -> np.ndarray:
+def decode_all_from_pool(r: Replayed, q: np.ndarray, scale: float,
+                         layer: int = 0) -> np.ndarray:
     """Oracle output for the whole batch, gathered through the oracle's own
-    block tables from the oracle's own pool copy (layer 0)."""
+    block tables from the oracle's own pool copy (one layer)."""
     assert r.data is not None
     m = r.model
     tables = [m.nodes[i].table for i in r.decode_ids]
     lens = [m.nodes[i].seq_len for i in r.decode_ids]
     if r.kv_dtype == "e4m3":
         return decode_step_fp8(q, r.data, tables, lens, scale,
-                               r.w.block_size)
-    return att.decode_step(q, r.data.k[0], r.data.v[0], tables, lens, scale,
+                               r.w.block_size, layer=layer)
+    return att.decode_step(q, r.data.k[layer], r.data.v[layer], tables, lens, scale,
                            r.w.block_size)

@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int bb = 0; bb < kTB; ++bb) {
         const float2 sr = lds64f(sS + sc * (kTB * 16) + bb * 16);
-        kf[bb] = fsc * sr.x;
+        kf[bb] = bb < nvb ? fsc * sr.x : 0.f;
         vsc[bb] = bb < nvb ? sr.y : 0.f;
         vmax = fmaxf(vmax, vsc[bb]);
       }
@@ -458,7 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c * 32 + i < valid)
               bm[i >> 4] = fmaxf(bm[i >> 4], __uint_as_float(sv[i]));
         }
-        mx = fmaxf(mx, fmaxf(bm[0] * kf[2 * c], bm[1] * kf[2 * c + 1]));
+        // Blocks past the item's range have no record in this stage (the
+        // slot holds whatever an earlier tile or kernel left there).
+        if (2 * c < nvb) mx = fmaxf(mx, bm[0] * kf[2 * c]);
+        if (2 * c + 1 < nvb) mx = fmaxf(mx, bm[1] * kf[2 * c + 1]);
       }
       const bool need = mx > m_used + kRescale;
       const float m_new = need ? mx : m_used;

@@ -131,9 +131,16 @@ def run_decode(cache, q_bits, flags=0):
 
 # ---- tests ---------------------------------------------------------------------
 
-@pytest.mark.parametrize("name", ["tiny_tree", "deep_tree", "fanout", "gqa_2"])
+def deep_tree_3_layers():
+    w = SMALL["deep_tree"]()
+    w.num_layers = 3
+    return w
+
+
+@pytest.mark.parametrize("name", ["tiny_tree", "deep_tree", "fanout", "gqa_2",
+                                  "deep_tree_3_layers"])
 def test_e4m3_pool_bit_exact(name):
-    w = SMALL[name]()
+    w = deep_tree_3_layers() if name == "deep_tree_3_layers" else SMALL[name]()
     cache = H.Cache(w, kv_dtype="e4m3")
     ref = rp.replay(w, with_data=True, kv_dtype="e4m3")
     assert cache.tables() == {i: (n.table, n.seq_len)
@@ -361,4 +368,39 @@ def test_e4m3_full_size_sampled_rows():
                          att.attention(qr, kq[:, g], vq[:, g], w.scale),
                          f"row {b} head group {g}")
     assert np.isfinite(gpu).all() and np.abs(gpu).max() < 8
+    cache.close()
+
+
+def test_e4m3_stale_shared_memory_does_not_leak():
+    """Shared memory left behind by an earlier kernel must not reach the
+    output.  A step over a pool whose every byte is 0xC0 (each 32-bit word
+    reads as -6.02) runs on every SM first; then a step whose segment tiles
+    end part-way through (deep_tree: ranges that are not a multiple of 8
+    blocks) must still match the oracle."""
+    junk_w = W.independent(n_seqs=64, min_len=1500, max_len=2500)
+    junk = H.Cache(junk_w, kv_dtype="e4m3")
+    junk.k.fill_(0xC0)
+    junk.v.fill_(0xC0)
+    junk.scales.view(torch.uint8).fill_(0xC0)
+    jq = junk_w.queries(len(junk.decode_ids))
+    jb = junk.batch().upload()
+    jout = torch.empty((len(junk.decode_ids), junk_w.Hq, junk_w.d),
+                       dtype=torch.bfloat16, device="cuda")
+    w = SMALL["deep_tree"]()
+    cache = H.Cache(w, kv_dtype="e4m3")
+    ref = rp.replay(w, with_data=True, kv_dtype="e4m3")
+    q = w.queries(len(cache.decode_ids))
+    bt = cache.batch().upload()
+    assert bt.info.n_tile_items > 0
+    out = torch.empty((len(cache.decode_ids), w.Hq, w.d), dtype=torch.bfloat16,
+                      device="cuda")
+    want = rp.decode_all_from_pool(ref, q, w.scale)
+    for _ in range(3):
+        jb.decode(bits_to_dev(jq), jout)
+        bt.decode(bits_to_dev(q), out)
+        torch.cuda.synchronize()
+        gpu = bf16_out(out)
+        assert np.isfinite(gpu).all()
+        assert_close(gpu, want, "after a junk step")
+    junk.close()
     cache.close()
