@@ -615,6 +615,36 @@ def run_ours(args):
                         "pinned host memory; best of 3",
             }
 
+    # The same step captured once into a CUDA graph and replayed: what an
+    # engine launching many layers per token would do; it removes the host's
+    # per-launch cost, which matters when the step itself is short.
+    graph = None
+    try:
+        qg = q.clone()
+        og = torch.empty_like(out)
+        bt.decode(qg, og)
+        torch.cuda.synchronize()
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg):
+            bt.decode(qg, og)
+        for _ in range(3):
+            cg.replay()
+        n_g = max(20, min(K, 500))
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        g0.record(stream)
+        for _ in range(n_g):
+            cg.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        ms_g = g0.elapsed_time(g1) / n_g
+        graph = {"ms_per_step": round(ms_g, 5),
+                 "value": round(uniq / (ms_g / 1e3) / 1e9, 1),
+                 "unit": "GB/s", "replays": n_g}
+    except RuntimeError as exc:          # capture unsupported: report why
+        graph = {"unavailable": str(exc)[:200]}
+
     # NEXT-3: the same step over an e4m3 copy of the workload's pool (codes
     # plus one 16-byte scale record per block and kv-head).
     e4m3 = None
@@ -754,6 +784,7 @@ def run_ours(args):
             "fused_append": fused,
             "radix_index": radix_timing(),
             "offload": offload,
+            "graph_replay": graph,
             "kv_e4m3": e4m3,
             "gpu_launches": launches_per_step * K,
             "clocks": clocks,
