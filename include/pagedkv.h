@@ -523,6 +523,17 @@ kv_status paged_decode_attn_noalloc(
 kv_status kv_check_device_status(void* workspace, void* stream,
                                  int32_t* out_code, int32_t* out_detail);
 
+/* Diagnostic: launch one thread that waits, bounded by wait_cycles SM clock
+ * cycles, on an mbarrier that nothing completes, then records KV_ERR_TIMEOUT
+ * (detail 99) in the status word of `workspace` exactly as the attention
+ * kernels do when one of their bounded waits runs out (their bound is 2^31
+ * cycles, about a second); kv_check_device_status then reports it.  It lets
+ * the timeout path be exercised without a fault or a hang.  workspace:
+ * device, 256-byte aligned, >= 256 bytes.  wait_cycles in [1, 2^31].
+ * Errors: INVALID_ARG, CUDA. */
+kv_status kv_selftest_timeout(void* workspace, int64_t wait_cycles,
+                              void* stream);
+
 /* Optional per-kernel timing (measurement support, not part of the method).
  * While set, each paged_decode_attn call on this thread records, on its
  * stream, events[2*i] just before and events[2*i+1] just after its kernel i:

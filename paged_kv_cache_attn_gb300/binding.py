@@ -152,6 +152,7 @@ _SIGS = {
                                                   C.POINTER(kv_decode_plan_info),
                                                   _vp, C.c_size_t, _vp]),
     "kv_check_device_status": (C.c_int32, [_vp, _vp, _i32p, _i32p]),
+    "kv_selftest_timeout": (C.c_int32, [_vp, C.c_int64, _vp]),
     "kv_offload_attach": (C.c_int32, [_vp, _vp, _vp, _vp, C.c_int64]),
     "kv_spill": (C.c_int32, [_vp, C.c_int32, _i32p, _vp, _i32p]),
     "kv_restore": (C.c_int32, [_vp, C.c_int32, _i32p, _vp, _i32p]),
@@ -489,6 +490,11 @@ def paged_decode_attn_noalloc(q, k_pool, v_pool, num_blocks, block_tables,
         _ptr(seq_lens), _ptr(prefix_groups), n_groups, nb, max_blocks, Hq, Hkv,
         head_dim, block_size, scale, _ptr(out), _ptr(plan), C.byref(info),
         _stream(stream)))
+
+
+def kv_selftest_timeout(workspace, wait_cycles, stream=None):
+    _check(_lib.kv_selftest_timeout(_ptr(workspace), wait_cycles,
+                                    _stream(stream)))
 
 
 def kv_check_device_status(workspace, stream=None):

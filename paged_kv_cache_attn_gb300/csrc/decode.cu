@@ -791,6 +791,35 @@ extern "C" kv_status paged_decode_append_attn(
                      workspace, ws_bytes, stream);
 }
 
+namespace pkv {
+namespace {
+// One thread waits on an mbarrier that nothing completes, with the same
+// bounded wait the attention kernels use, then records the timeout.
+__global__ void selftest_timeout_kernel(DeviceStatus* status, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  mbar_init(smem_u32(&bar), 1);
+  fence_mbar_init();
+  if (!mbar_wait_for(smem_u32(&bar), 0, limit))
+    record_status(status, KV_ERR_TIMEOUT, 99);
+}
+}  // namespace
+}  // namespace pkv
+
+extern "C" kv_status kv_selftest_timeout(void* workspace, int64_t wait_cycles,
+                                         void* stream) {
+  pkv::clear_error();
+  if (!workspace || ((uintptr_t)workspace & 255))
+    return fail(KV_ERR_INVALID_ARG, "workspace: non-null, 256-byte aligned");
+  if (wait_cycles < 1 || wait_cycles > pkv::kWaitCycles)
+    return fail(KV_ERR_INVALID_ARG, "wait_cycles outside [1, 2^31]");
+  pkv::selftest_timeout_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(
+      static_cast<pkv::DeviceStatus*>(workspace), wait_cycles);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return fail(KV_ERR_CUDA, "self-test launch: %s", cudaGetErrorString(e));
+  return KV_OK;
+}
+
 extern "C" kv_status kv_check_device_status(void* workspace, void* stream,
                                             int32_t* out_code,
                                             int32_t* out_detail) {
