@@ -459,6 +459,35 @@ kv_status make_pool_map(CUtensorMap* tm, const void* pool, int64_t rows, int d) 
   return KV_OK;
 }
 
+// 5-D view of one layer's pool (head_dim 128) in which one box is a whole
+// (block, kv-head) tile of 16 rows x 128 columns:
+//   x0: column within a 64-column half (2 bytes)   box 64
+//   x1: row within a group of 8        (256 bytes) box 8
+//   x2: column half                    (128 bytes) box 2
+//   x3: group of 8 rows                (2048 bytes) box 2
+//   x4: block * Hkv + head             (4096 bytes) box 1
+// The strides are not nested (x2 steps inside a row), which a load allows;
+// every coordinate inside the dims addresses the tile's own 4 KB.  With
+// 128-byte swizzle the box lands as four 1 KB atoms of 8 rows x 64 columns,
+// ordered (group 0, half 0), (0, 1), (1, 0), (1, 1): the canonical K-major
+// layout with 8-row groups 2048 bytes apart and halves 1024 bytes apart.
+kv_status make_pool_map_tiles(CUtensorMap* tm, const void* pool, int64_t nh) {
+  auto enc = get_encode();
+  if (!enc) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[5] = {64, 8, 2, 2, (cuuint64_t)nh};
+  cuuint64_t strides[4] = {256, 128, 2048, 4096};
+  cuuint32_t box[5] = {64, 8, 2, 2, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
+                   const_cast<void*>(pool), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled (tiles) failed (%d)", (int)r);
+  return KV_OK;
+}
+
 template <int D>
 cudaError_t launch_split(const CUtensorMap& tk, const CUtensorMap& tv,
                          const SplitParams& sp, int n_items,
@@ -609,11 +638,17 @@ static kv_status decode_impl(
                 ws_bytes, need);
 
   cudaStream_t st = (cudaStream_t)stream;
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tk_tiles, tv_tiles;
   const int64_t rows = num_blocks * Hkv * 16;
   if (!e4m3) {
     if (kv_status s = pkv::make_pool_map(&tk, k_pool, rows, d)) return s;
     if (kv_status s = pkv::make_pool_map(&tv, v_pool, rows, d)) return s;
+    if (info->n_tile_items > 0) {
+      if (kv_status s = pkv::make_pool_map_tiles(&tk_tiles, k_pool, num_blocks * Hkv))
+        return s;
+      if (kv_status s = pkv::make_pool_map_tiles(&tv_tiles, v_pool, num_blocks * Hkv))
+        return s;
+    }
   }
 
   auto* ws = static_cast<uint8_t*>(workspace);
@@ -671,7 +706,8 @@ static kv_status decode_impl(
     const auto* titems = reinterpret_cast<const pkv::WorkItem*>(plan + off_tile);
     e = e4m3 ? pkv::launch_tile_e4m3(sp, titems, info->n_tile_items, k_pool,
                                      v_pool, kv_scales, ts)
-             : pkv::launch_tile_items(tk, tv, sp, titems, info->n_tile_items, d,
+             : pkv::launch_tile_items(tk_tiles, tv_tiles, sp, titems,
+                                      info->n_tile_items, d,
                                       info->tile_cluster, ts);
     pkv::mark(1, ts);
     if (e != cudaSuccess)

@@ -9,18 +9,23 @@
 // enough (up to 128 flops per KV byte) to belong on the tensor cores.
 //
 // Pipeline per 128-token KV tile j (8 blocks of 16):
-//   warps 5-8 (TMA):   K and V, each as two column halves: 8 boxes (16 rows
-//                      x 64 cols, 128-byte swizzle) per warp and tile, one
-//                      per lane, into stage j % 2 -> k_full / v_full
+//   warps 5-8 (TMA):   K and V, each a box per (block, kv-head) tile (16
+//                      rows x 128 cols as four 1 KB atoms of 8 rows x 64
+//                      cols, 128-byte swizzle), into stage j % kNS ->
+//                      k_full / v_full
 //   warp 4  (MMA):     S[j%2] = Q K^T  (M=128, N=128, K=128; Q and S in
 //                      TMEM) -> s_full, k_empty; then O += P(j-1) V(j-1)
 //                      (M=128, N=128, K=128; P in TMEM, V as an MN-major
 //                      shared-memory operand) -> v_empty, pv_done
 //   warps 0-3 (rows):  thread r owns row r: two passes over its S row in
-//                      TMEM (maximum, then P = 2^(s - m) as bf16 pairs into
-//                      TMEM), base-2 online softmax with a lazy maximum (O and
-//                      l are rescaled only when the row maximum grows by more
-//                      than 8, so p <= 256) -> p_full
+//                      TMEM (maximum, then P = 2^(s - m) as bf16 pairs over
+//                      the first 64 columns of the same S buffer), base-2
+//                      online softmax with a lazy maximum (O and l are
+//                      rescaled only when the row maximum grows by more than
+//                      8, so p <= 256) -> p_full.  Only a rescale of O waits
+//                      for PV(j-1); otherwise the softmax of tile j overlaps
+//                      it.  The MMAs of one thread run in issue order, so
+//                      QK(j+2), which overwrites S[j%2], follows PV(j).
 // An MMA of M=128, K=16 costs about the same ~95 cycles for N=64 and N=128
 // on this part, so 128-token tiles halve the QK cost per token.
 // At the end the rows read O from TMEM and write unnormalised partials
@@ -37,16 +42,18 @@ namespace tc {
 
 constexpr int kT = 128;                  // tokens per KV tile
 constexpr int kTB = kT / 16;             // blocks per KV tile
-constexpr int kNS = 2;                   // stages of each of the K and V rings
-constexpr int kBox = kT * 128;           // one 64-column box of a K/V tile
+constexpr int kNS = 3;                   // stages of each of the K and V rings
+constexpr int kBlk = 16 * 128 * 2;       // one (block, kv-head) tile: a box
+constexpr int kBox = kT * 128;           // bytes a producer warp loads a tile
 constexpr int kKV = 2 * kBox;            // K (or V) tile, head_dim 128
 constexpr int kSmem = 2 * kNS * kKV + 1024;
 constexpr int kThreads = 288;            // warps 0-3 rows, 4 MMA, 5-8 TMA
 constexpr int kMmaWarp = 4;
-// TMEM columns (fp32 unless noted): S[0] 0..127, S[1] 128..255, P 256..319
-// (bf16 pairs), O 320..447, Q 448..511 (bf16 pairs).
+// TMEM columns (fp32 unless noted): S[0] 0..127, S[1] 128..255 (P of a tile
+// overwrites the first 64 columns of its S buffer as bf16 pairs), O
+// 320..447, Q 448..511 (bf16 pairs).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColP = 256, kColO = 320, kColQ = 448;
+constexpr uint32_t kColO = 320, kColQ = 448;
 constexpr float kRescale = 8.f;          // lazy-max threshold (log2 units)
 constexpr int kTblWin = 128;             // block-table entries staged at once
 
@@ -64,7 +71,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tile_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
                        const SplitParams p, const WorkItem* items,
-                       int64_t oob_row, int cluster) {
+                       int oob_tile, int cluster) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) Bars bars;
   __shared__ uint32_t tmem_base_sh;
@@ -172,20 +179,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base_sh;
 
   if (warp >= 5) {
-    // ---- TMA producers: warp 5 / 6 = K column half 0 / 1, warp 7 / 8 = V.
-    // Each issues its half of a tile's 4 blocks from lanes 0-3 in one
-    // instruction.  A single thread issuing boxes back to back costs ~180
-    // cycles a box, so four warps share the 16 boxes of a tile.  A K stage
-    // frees as soon as its QK product is done, a V stage after its PV
-    // product; K and V producers run independently.  Block-table entries are
-    // staged in shared memory, kTblWin at a time, with coalesced loads.
+    // ---- TMA producers: warps 5 / 6 = K blocks 0-3 / 4-7 of a tile, warps
+    // 7 / 8 = V.  One box is a whole (block, kv-head) tile of 4 KB; a warp
+    // issues its blocks from lanes 0-3 (0-1 in a pair, which splits them) in
+    // one instruction.  A K stage frees as soon as its QK product is done, a
+    // V stage after its PV product; K and V producers run independently.
+    // Block-table entries are staged in shared memory, kTblWin at a time,
+    // with coalesced loads.
     const int pw = warp - 5;
     const bool is_v = pw >= 2;
     const int half = pw & 1;
     const CUtensorMap* tm = is_v ? &tmV : &tmK;
     uint64_t* full = is_v ? bars.v_full : bars.k_full;
     uint64_t* empty = is_v ? bars.v_empty : bars.k_empty;
-    const uint32_t ring = (is_v ? sV : sK) + half * kBox;
+    const uint32_t ring = is_v ? sV : sK;
     int* tbl = tbl_sh[pw];
     int issued = 0, win = -1;
     bool ok = true;
@@ -209,21 +216,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      if (lane < kTB / cluster) {
-        const int rel = j * kTB + lane * cluster + (int)crank;
-        int64_t y = oob_row;  // zero fill past the range
+      if (lane < kTB / 2 / cluster) {
+        const int bi = half * (kTB / 2) + lane * cluster + (int)crank;
+        const int rel = j * kTB + bi;
+        int y = oob_tile;  // zero fill past the range
         if (it.blk_begin + rel < it.blk_end) {
           const int phys = tbl[rel - win];
           if (phys >= 0 && (int64_t)phys < p.num_blocks)
-            y = ((int64_t)phys * p.Hkv + it.g) * 16;
+            y = phys * p.Hkv + it.g;
           else if (pw == 0)
             record_status(p.status, KV_ERR_DEVICE, phys);
         }
-        const uint32_t dst = ring + s * kKV + (rel - j * kTB) * 2048;
+        const uint32_t dst = ring + s * kKV + bi * kBlk;
         if (cluster > 1)
-          tma_load_2d_mc(dst, tm, half * 64, (int)y, smem_u32(&full[s]), cmask);
+          tma_load_5d_mc(dst, tm, y, smem_u32(&full[s]), cmask);
         else
-          tma_load_2d(dst, tm, half * 64, (int)y, smem_u32(&full[s]));
+          tma_load_5d(dst, tm, y, smem_u32(&full[s]));
       }
       __syncwarp();
       issued = j + 1;
@@ -251,8 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vst = sV + s * kKV;
 #pragma unroll
         for (int kt = 0; kt < kT / 16; ++kt) {
-          const uint64_t bd = sdesc(vst + kt * 2048, kBox, 1024);
-          umma_ts(tmem + kColO, tmem + kColP + kt * 8, bd, id_pv,
+          const uint64_t bd = sdesc(vst + kt * kBlk, 1024, 2048);
+          umma_ts(tmem + kColO, tmem + (jp & 1) * kT + kt * 8, bd, id_pv,
                   (jp > 0 || kt > 0) ? 1u : 0u);
         }
         if (cluster > 1)
@@ -272,8 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kst = sK + s * kKV;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = sdesc(kst + (kk >> 2) * kBox + (kk & 3) * 32, 16,
-                                    1024);
+          const uint64_t bd = sdesc(kst + (kk >> 2) * 1024 + (kk & 3) * 32, 16,
+                                    2048);
           umma_ts(tmem + b * kT, tmem + kColQ + kk * 8, bd, id_qk,
                   kk > 0 ? 1u : 0u);
         }
@@ -334,16 +342,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float alpha = need ? ex2(m_used - m_new) : 1.f;
       l *= alpha;
       m_used = m_new;
-      // Pass 2: P = 2^(s * scale_log2 - m) as bf16 pairs, kept in registers
-      // while PV(j - 1) may still be reading the P columns.
+      // Pass 2: P = 2^(s * scale_log2 - m) as bf16 pairs, written over the
+      // first 64 columns of this tile's own S buffer: chunk c of P lands on
+      // columns 16c .. 16c + 15, which this thread has already read.
       const float neg_m = -m_used;
-      uint32_t pk[kT / 2];
 #pragma unroll
       for (int c = 0; c < kT / 32; ++c) {
         uint32_t sv[32];
         tmem_ld32(srow + c * 32, sv);
         tmem_wait_ld();
         float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int t0 = c * 32 + 2 * i;
@@ -352,18 +361,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           p0 = t0 < valid ? p0 : 0.f;
           p1 = t0 + 1 < valid ? p1 : 0.f;
           acc4[i & 3] += p0 + p1;
-          pk[c * 16 + i] = pack_bf16(p0, p1);
+          pk[i] = pack_bf16(p0, p1);
         }
         l += (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+        tmem_st16(srow + c * 16, pk);
       }
-      // P and O are free of PV(j - 1) once it is done (one P buffer).
-      if (j > 0 && !mbar_wait(smem_u32(&bars.pv_done), (j - 1) & 1)) {
-        ok = false;
-        break;
-      }
-      fence_after_sync();
       if (__any_sync(0xffffffffu, need) && j > 0) {
-        // Rescale this row of O (it holds PV up to tile j - 1).
+        // Rescale this row of O (it holds PV up to tile j - 1) once PV(j - 1)
+        // is done.  PV(j) cannot have started (it waits for this tile's P),
+        // so the barrier has completed j - 1 or j phases and the parity wait
+        // is exact.
+        if (!mbar_wait(smem_u32(&bars.pv_done), (j - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t ov[32];
@@ -374,13 +386,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
           tmem_st32(lane_base + kColO + c * 32, ov);
         }
-      }
-#pragma unroll
-      for (int c = 0; c < kT / 32; ++c) {
-        uint32_t q16[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) q16[i] = pk[c * 16 + i];
-        tmem_st16(lane_base + kColP + c * 16, q16);
       }
       tmem_wait_st();
       fence_before_sync();
@@ -444,8 +449,9 @@ cudaError_t launch_tile_items(const CUtensorMap& tk, const CUtensorMap& tv,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  // A row past the end of the pool's 2-D view: TMA fills the box with zeros.
-  const int64_t oob_row = sp.num_blocks * sp.Hkv * 16;
+  // A (block, head) index past the end of the pool: TMA fills with zeros.
+  if ((int64_t)sp.num_blocks * sp.Hkv > INT32_MAX - 1) return cudaErrorInvalidValue;
+  const int oob_tile = (int)((int64_t)sp.num_blocks * sp.Hkv);
   if (cluster < 1 || cluster > 2 || n_items % cluster != 0)
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
@@ -461,7 +467,7 @@ cudaError_t launch_tile_items(const CUtensorMap& tk, const CUtensorMap& tv,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, tc::tile_decode_kernel, tk, tv, sp, items,
-                            oob_row, cluster);
+                            oob_tile, cluster);
 }
 
 }  // namespace pkv

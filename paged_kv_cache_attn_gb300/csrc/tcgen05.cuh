@@ -89,6 +89,27 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* 
       : "memory");
 }
 
+// 5-D TMA load (coordinates x0..x4) into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* tm,
+                                            int x4, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%2, %2, %2, %2, %3}], [%4];" ::"r"(dst),
+      "l"(tm), "r"(0), "r"(x4), "r"(bar)
+      : "memory");
+}
+
+// The same written to the same offset in every CTA of `mask`.
+__device__ __forceinline__ void tma_load_5d_mc(uint32_t dst, const CUtensorMap* tm,
+                                               int x4, uint32_t bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::"
+      "bytes.multicast::cluster [%0], [%1, {%2, %2, %2, %2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(tm), "r"(0), "r"(x4), "r"(bar), "h"(mask)
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
