@@ -9,7 +9,10 @@
 // Split-KV kernel (one CTA = one work item = up to 16 query rows x one
 // kv-head x a range of logical blocks):
 //  * 4 warps; warp w takes blocks w, w + 4, ... of the range.  Each warp runs
-//    its own 3-stage ring (two CTAs fit on an SM): per block, lanes 0-3 each
+//    its own 2-stage ring, so that three CTAs fit on an SM (measured: three
+//    CTAs with two stages beat two CTAs with three stages, since a third
+//    item per SM hides more of each item's start-up and epilogue, which
+//    dominate short items): per block, lanes 0-3 each
 //    issue one 2-D TMA box (16 rows x 64 columns, 128-byte swizzle) of the
 //    (block, kv-head) K and V tiles, completing on the stage's mbarrier; the
 //    whole warp waits on it.
@@ -50,7 +53,7 @@ struct SplitCfg {
 };
 
 template <int D, int NS>
-__global__ void __launch_bounds__(128, 2)
+__global__ void __launch_bounds__(128, 3)
     splitkv_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV,
                           const SplitParams p) {
@@ -424,7 +427,7 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const MergeParams p) {
 
 namespace {
 
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
