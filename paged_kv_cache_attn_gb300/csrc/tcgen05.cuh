@@ -49,22 +49,10 @@ __device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a,
       : "memory");
 }
 
-// Instruction descriptor with A and B both K-major and format code 0 (f16 for
-// kind::f16, e4m3 for kind::f8f6f4), fp32 accumulator.
+// Instruction descriptor for kind::f16 with A and B both K-major and f16
+// (format code 0), fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_k0(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-// D (+)= A B with 8-bit A and B from shared memory (kind::f8f6f4, K = 32).
-__device__ __forceinline__ void umma_f8(uint32_t tmem_d, uint64_t a, uint64_t b,
-                                        uint32_t id, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(
-          tmem_d),
-      "l"(a), "l"(b), "r"(id), "r"(accumulate)
-      : "memory");
 }
 
 // Arrive on the mbarrier at this offset in every CTA of `mask` once this
