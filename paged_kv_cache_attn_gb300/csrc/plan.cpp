@@ -83,8 +83,11 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   // The tcgen05 tile kernels are built for head_dim 128 (bf16 and e4m3).
   const bool allow_tc = pkv::kTensorCoreKernel && d == 128 &&
                         !(flags & KV_PLAN_NO_TENSOR_CORES);
+  units.reserve((size_t)(use_groups ? n_groups : 0) + nb);
   if (use_groups && n_groups > 0) {
-    std::vector<std::vector<std::pair<int32_t, int32_t>>> per_row(nb);
+    // Each row's segment ranges, grouped by row with a counting sort (one
+    // flat array instead of a vector per row).
+    std::vector<int32_t> first(nb + 1, 0);
     for (int32_t i = 0; i < n_groups; ++i) {
       const int32_t* s = groups + 4 * (int64_t)i;
       const int32_t bb = s[0], bc = s[1], kb = s[2], kc = s[3];
@@ -97,21 +100,29 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
         if ((int64_t)(kb + kc) * B > seq_lens[b])
           return fail(KV_ERR_INVALID_ARG,
                       "segment %d covers a block not full for row %d", i, b);
-        per_row[b].push_back({kb, kb + kc});
+        ++first[b + 1];
       }
       units.push_back({bb, bc * G, kb, kb + kc, 0,
                        allow_tc && bc * G >= pkv::kMinTensorRows});
     }
+    for (int32_t b = 0; b < nb; ++b) first[b + 1] += first[b];
+    std::vector<std::pair<int32_t, int32_t>> ranges(first[nb]);
+    std::vector<int32_t> next(first.begin(), first.end() - 1);
+    for (int32_t i = 0; i < n_groups; ++i) {
+      const int32_t* s = groups + 4 * (int64_t)i;
+      for (int32_t b = s[0]; b < s[0] + s[1]; ++b)
+        ranges[next[b]++] = {s[2], s[2] + s[3]};
+    }
     for (int32_t b = 0; b < nb; ++b) {
-      auto& v = per_row[b];
-      std::sort(v.begin(), v.end());
+      auto lo_it = ranges.begin() + first[b], hi_it = ranges.begin() + first[b + 1];
+      std::sort(lo_it, hi_it);
       int32_t end = 0;
-      for (auto& [lo, hi] : v) {
-        if (lo != end)
+      for (auto it = lo_it; it != hi_it; ++it) {
+        if (it->first != end)
           return fail(KV_ERR_INVALID_ARG,
                       "row %d: segments do not tile [0, end) (gap or overlap "
-                      "at block %d)", b, lo);
-        end = hi;
+                      "at block %d)", b, it->first);
+        end = it->second;
       }
       shared_end[b] = end;
     }
@@ -145,6 +156,24 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   std::vector<pkv::WorkItem> row_items, tile_items;
   struct Tagged { int32_t branch; pkv::MergeEntry e; };
   std::vector<Tagged> merge_flat;
+  {
+    // Exact item counts and a bound on the merge entries, so that the loop
+    // below never reallocates.
+    int64_t n_row = 0, n_tile = 0, n_merge = 0;
+    for (const Unit& u : units) {
+      const int rows_per = u.tile ? pkv::kTileRows : pkv::kRowTile;
+      const int64_t nch =
+          ceil_div(u.blk_end - u.blk_begin, u.tile ? chunk_tile : chunk_rows);
+      const int64_t tiles = u.tile && tile_cluster == 2
+                                ? 2 * ceil_div(u.rows, 2 * rows_per)
+                                : ceil_div(u.rows, rows_per);
+      (u.tile ? n_tile : n_row) += nch * tiles * Hkv;
+      n_merge += nch * tiles * (rows_per / G + 2);
+    }
+    row_items.reserve(n_row);
+    tile_items.reserve(n_tile);
+    merge_flat.reserve(n_merge);
+  }
   int64_t prow = 0;
   for (const Unit& u : units) {
     const int rows_per = u.tile ? pkv::kTileRows : pkv::kRowTile;
