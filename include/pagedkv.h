@@ -385,6 +385,11 @@ typedef struct kv_decode_plan_info {
                               with 2, the two 128-row tiles of one segment
                               share every K/V load (TMA multicast) */
   int32_t flags;           /* the KV_PLAN_* flags the plan was made with */
+  int32_t n_row_warp_items; /* the last n_row_warp_items of the split-KV
+                               items are short (at most 16 blocks): the bf16
+                               split-KV kernel runs them four to a CTA, one
+                               per warp; the others take a whole CTA */
+  int32_t reserved;        /* 0 */
 } kv_decode_plan_info;
 
 /* Host half of a decode step: split the step into work items.

@@ -64,7 +64,8 @@ class kv_decode_plan_info(C.Structure):
                 ("partial_rows", C.c_int64), ("n_row_items", C.c_int32),
                 ("n_tile_items", C.c_int32), ("n_merge_rows", C.c_int32),
                 ("chunk_blocks", C.c_int32), ("tile_cluster", C.c_int32),
-                ("flags", C.c_int32)]
+                ("flags", C.c_int32), ("n_row_warp_items", C.c_int32),
+                ("reserved", C.c_int32)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

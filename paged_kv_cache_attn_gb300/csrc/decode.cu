@@ -52,11 +52,14 @@ struct SplitCfg {
       (kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes) + 1024;
 };
 
+// CTAs 0 .. n_long - 1 take items 0 .. n_long - 1 with all four warps; each
+// later CTA takes four of the remaining (short) items, one per warp, and its
+// warps write their partial rows themselves.
 template <int D, int NS>
 __global__ void __launch_bounds__(128, 3)
     splitkv_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV,
-                          const SplitParams p) {
+                          const SplitParams p, int n_long, int n_items) {
   using C = SplitCfg<D, NS>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[C::kWarps][NS];
@@ -68,11 +71,17 @@ __global__ void __launch_bounds__(128, 3)
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   float* base_ptr = reinterpret_cast<float*>(
       smem_raw + (base - smem_u32(smem_raw)));
-  const WorkItem it = p.items[blockIdx.x];
-  if (!item_ok(it, p, 16)) {
-    if (threadIdx.x == 0) record_status(p.status, KV_ERR_DEVICE, -1 - (int)blockIdx.x);
-    return;
+  const bool per_warp = (int)blockIdx.x >= n_long;  // uniform in the CTA
+  const int idx = per_warp ? n_long + 4 * ((int)blockIdx.x - n_long) + warp
+                           : (int)blockIdx.x;
+  WorkItem it = p.items[idx < n_items ? idx : 0];
+  bool have = idx < n_items;
+  if (have && !item_ok(it, p, 16)) {
+    if (per_warp ? lane == 0 : threadIdx.x == 0)
+      record_status(p.status, KV_ERR_DEVICE, -1 - idx);
+    have = false;
   }
+  if (!per_warp && !have) return;  // the whole CTA, before any barrier
 
   if (threadIdx.x == 0) {
     for (int w = 0; w < C::kWarps; ++w)
@@ -83,11 +92,15 @@ __global__ void __launch_bounds__(128, 3)
   }
   __syncthreads();
 
+  if (!have) return;  // a warp without an item (no CTA barrier follows)
   const int G = p.G;
   const int seq_len = it.masked ? p.seq_lens[it.branch0] : 0x7fffffff;
   const int32_t* table = p.tables + (int64_t)it.branch0 * p.max_blocks;
   const int nblk = it.blk_end - it.blk_begin;
-  const int my_n = nblk > warp ? (nblk - warp + C::kWarps - 1) / C::kWarps : 0;
+  // This warp's blocks of the item: first, first + stride, ...
+  const int first = per_warp ? 0 : warp;
+  const int stride = per_warp ? 1 : C::kWarps;
+  const int my_n = nblk > first ? (nblk - first + stride - 1) / stride : 0;
   const uint32_t ring = base + warp * NS * C::kStageBytes;
   const uint32_t bar0 = smem_u32(&bars[warp][0]);
 
@@ -101,7 +114,7 @@ __global__ void __launch_bounds__(128, 3)
     if ((k >> 5) != twin) {
       twin = k >> 5;
       const int kk = (twin << 5) + lane;
-      tcache = kk < my_n ? table[it.blk_begin + warp + C::kWarps * kk] : 0;
+      tcache = kk < my_n ? table[it.blk_begin + first + stride * kk] : 0;
     }
     const int phys = __shfl_sync(0xffffffffu, tcache, k & 31);
     const bool ok = phys >= 0 && (int64_t)phys < p.num_blocks;
@@ -180,7 +193,7 @@ __global__ void __launch_bounds__(128, 3)
       timed_out = true;
       break;
     }
-    const int j = it.blk_begin + warp + C::kWarps * k;
+    const int j = it.blk_begin + first + stride * k;
     if (!((bad >> s) & 1)) {
       int nv = seq_len - j * 16;
       nv = nv > 16 ? 16 : nv;
@@ -309,6 +322,28 @@ __global__ void __launch_bounds__(128, 3)
   for (int hr = 0; hr < 2; ++hr) {
     l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], 1);
     l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], 2);
+  }
+
+  if (per_warp) {
+    // The warp's own item: its state is the partial result.  Lane (gq, tq)
+    // holds rows gq and gq + 8, columns 8 nt + 2 tq and + 1.
+    float* dst = p.o + (int64_t)it.prow_base * D;
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) {
+      const int col = nt * 8 + 2 * tq;
+      if (gq < it.nrows)
+        *reinterpret_cast<float2*>(dst + gq * D + col) =
+            make_float2(o[nt][0], o[nt][1]);
+      if (gq + 8 < it.nrows)
+        *reinterpret_cast<float2*>(dst + (gq + 8) * D + col) =
+            make_float2(o[nt][2], o[nt][3]);
+    }
+    if (tq == 0) {
+      if (gq < it.nrows) p.ml[it.prow_base + gq] = make_float2(m_r[0], l_r[0]);
+      if (gq + 8 < it.nrows)
+        p.ml[it.prow_base + gq + 8] = make_float2(m_r[1], l_r[1]);
+    }
+    return;
   }
 
   // Combine the four warps' partial states through shared memory.
@@ -493,8 +528,10 @@ kv_status make_pool_map_tiles(CUtensorMap* tm, const void* pool, int64_t nh) {
 
 template <int D>
 cudaError_t launch_split(const CUtensorMap& tk, const CUtensorMap& tv,
-                         const SplitParams& sp, int n_items,
+                         const SplitParams& sp, int n_items, int n_warp_items,
                          cudaStream_t stream) {
+  if (n_warp_items < 0 || n_warp_items > n_items) return cudaErrorInvalidValue;
+  const int n_long = n_items - n_warp_items;
   using C = SplitCfg<D, kStages>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -504,8 +541,9 @@ cudaError_t launch_split(const CUtensorMap& tk, const CUtensorMap& tv,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  splitkv_decode_kernel<D, kStages><<<n_items, 128, C::kSmem, stream>>>(tk, tv,
-                                                                        sp);
+  splitkv_decode_kernel<D, kStages>
+      <<<n_long + (n_warp_items + 3) / 4, 128, C::kSmem, stream>>>(
+          tk, tv, sp, n_long, n_items);
   return cudaGetLastError();
 }
 
@@ -635,6 +673,9 @@ static kv_status decode_impl(
     return fail(KV_ERR_INVALID_ARG, "scale must be finite and > 0");
   if (info->n_merge_rows != nb || info->partial_rows < 0)
     return fail(KV_ERR_INVALID_ARG, "plan info does not match nb");
+  if (info->n_row_warp_items < 0 || info->n_row_warp_items > info->n_row_items)
+    return fail(KV_ERR_INVALID_ARG, "plan info: bad n_row_warp_items %d",
+                info->n_row_warp_items);
   const size_t need = pkv::ws_total(info->partial_rows, d);
   if (ws_bytes < need || (size_t)info->workspace_bytes != need)
     return fail(KV_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed",
@@ -728,8 +769,10 @@ static kv_status decode_impl(
       e = pkv::launch_split_e4m3(sp, k_pool, v_pool, kv_scales,
                                  info->n_row_items, d, st);
     else
-      e = d == 128 ? pkv::launch_split<128>(tk, tv, sp, info->n_row_items, st)
-                   : pkv::launch_split<64>(tk, tv, sp, info->n_row_items, st);
+      e = d == 128 ? pkv::launch_split<128>(tk, tv, sp, info->n_row_items,
+                                            info->n_row_warp_items, st)
+                   : pkv::launch_split<64>(tk, tv, sp, info->n_row_items,
+                                           info->n_row_warp_items, st);
     pkv::mark(3, st);
     if (e != cudaSuccess)
       return fail(KV_ERR_CUDA, "split-KV kernel: %s", cudaGetErrorString(e));

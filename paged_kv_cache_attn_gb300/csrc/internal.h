@@ -92,6 +92,7 @@ constexpr bool kTensorCoreKernel = true;  // tcgen05 tile kernel available
 constexpr int kTileRows = 128;      // rows of a tcgen05 tile
 constexpr int kRowTile = 16;        // rows of an mma.sync tile
 constexpr int kMinTensorRows = 65;  // segments with more rows go to tcgen05
+constexpr int kWarpItemBlocks = 16; // split-KV items this short run per warp
 
 // Workspace layout (bytes): status word block, then (m, l) pairs, then o rows.
 constexpr size_t kStatusBytes = 256;

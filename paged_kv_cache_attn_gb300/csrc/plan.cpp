@@ -234,6 +234,14 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
       }
     }
   }
+  // Short split-KV items go last (stable): the bf16 split-KV kernel runs
+  // them one per warp, four to a CTA.  An item's partial rows do not depend
+  // on its position, so the merge lists stand.
+  const auto first_short = std::stable_partition(
+      row_items.begin(), row_items.end(), [](const pkv::WorkItem& it) {
+        return it.blk_end - it.blk_begin > pkv::kWarpItemBlocks;
+      });
+  const int32_t n_warp_items = (int32_t)(row_items.end() - first_short);
   const int64_t n_csr = (int64_t)merge_flat.size();
   const int64_t off_row = pkv::kPlanHeaderInts;
   const int64_t off_tile = off_row + 8 * (int64_t)row_items.size();
@@ -246,6 +254,8 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   info->partial_rows = prow;
   info->workspace_bytes = (int64_t)pkv::ws_total(prow, d);
   info->n_row_items = (int32_t)row_items.size();
+  info->n_row_warp_items = n_warp_items;
+  info->reserved = 0;
   info->n_tile_items = (int32_t)tile_items.size();
   info->n_merge_rows = nb;
   info->chunk_blocks = chunk_rows;

@@ -297,6 +297,28 @@ def test_plan_covers_every_token_once(name, flags):
             assert total == nblk[b]
     if flags & B.KV_PLAN_IGNORE_GROUPS:
         assert (rows[:, 7] == 1).all()
+    # The split-KV items of at most 16 blocks come last, counted in the info.
+    nw = bt.info.n_row_warp_items
+    span = rows[:, 5] - rows[:, 4]
+    assert 0 <= nw <= len(rows)
+    assert (span[len(rows) - nw:] <= 16).all()
+    assert (span[:len(rows) - nw] > 16).all()
+
+
+def test_short_split_items_keep_their_order():
+    """The short items are moved behind the long ones without reordering
+    either group (a stable partition), and every item is still there."""
+    w = W.make("deep_tree")
+    bt = H.Cache(w, with_data=False).batch(num_sms=152)
+    rows, _, _, _ = decode_plan(bt.plan, bt.info, bt.nb, w.Hq, w.Hkv)
+    nw = bt.info.n_row_warp_items
+    assert nw > 1000                       # most deep_tree items are short
+    # Partial-row bases were handed out in generation order, so each group
+    # must still be in increasing base order.
+    base = rows[:, 6]
+    assert (np.diff(base[:len(rows) - nw]) > 0).all()
+    assert (np.diff(base[len(rows) - nw:]) > 0).all()
+    assert sorted(base.tolist()) == sorted(set(base.tolist()))
 
 
 def test_multi_tile_segments_run_as_pairs():
