@@ -12,6 +12,7 @@
 struct Node {
   int32_t parent = -1;
   int32_t depth = 0;
+  int32_t inherited = 0;  // full blocks shared with the parent at the fork
   int32_t seq_len = 0;
   bool live = true;
   int32_t spilled = 0;  // table entries held in the host tier

@@ -398,6 +398,7 @@ extern "C" kv_status kv_fork_branches(kv_pool* p, int32_t parent, int32_t n,
     Node c;
     c.parent = parent;
     c.depth = depth;
+    c.inherited = full;
     c.seq_len = seq_len;
     c.table = shared;
     for (int32_t b : shared) p->ref[b] += 1;
@@ -669,6 +670,29 @@ extern "C" kv_status kv_build_batch(kv_pool* p, int32_t nb, const int32_t* ids,
     rows[b] = nd;
   }
   const int32_t B = p->block_size;
+  // A lower bound on the common prefix of two branches' tables, in blocks,
+  // from fork ancestry: a child shares its parent's full blocks at the fork,
+  // and those entries never change while both branches hold them (full
+  // blocks are immutable, and a block held twice is never spilled or moved).
+  // So two branches agree on the smallest such count along their paths to
+  // their lowest common ancestor.  Branches with no common ancestor (e.g.
+  // made from the radix index) get 0, and the comparison below does the rest.
+  auto ancestry_floor = [&](int32_t a, int32_t c) -> int32_t {
+    int32_t fa = INT32_MAX, fc = INT32_MAX;
+    while (a != c) {
+      if (a < 0 || c < 0) return 0;
+      const Node& na = p->nodes[a];
+      const Node& nc = p->nodes[c];
+      if (na.depth >= nc.depth) {
+        fa = std::min(fa, na.inherited);
+        a = na.parent;
+      } else {
+        fc = std::min(fc, nc.inherited);
+        c = nc.parent;
+      }
+    }
+    return std::min(fa, fc);
+  };
   std::vector<int32_t> lcp(nb > 1 ? nb - 1 : 0);
   for (int32_t i = 0; i + 1 < nb; ++i) {
     const Node* a = rows[i];
@@ -676,7 +700,7 @@ extern "C" kv_status kv_build_batch(kv_pool* p, int32_t nb, const int32_t* ids,
     const int32_t lim = std::min(a->seq_len / B, c->seq_len / B);
     const int32_t* x = a->table.data();
     const int32_t* y = c->table.data();
-    int32_t j = 0;
+    int32_t j = std::min(ancestry_floor(ids[i], ids[i + 1]), lim);
     // Whole 64-entry chunks with memcmp, then entry by entry.
     while (j + 64 <= lim && std::memcmp(x + j, y + j, 64 * sizeof(int32_t)) == 0)
       j += 64;
