@@ -110,6 +110,21 @@ def test_decode_refuses_a_plan_for_the_other_element_type():
         info_e8.workspace_bytes)) == B.KV_ERR_INVALID_ARG
 
 
+def test_decode_refuses_a_bad_short_item_count():
+    """The count of short split items (run one per warp) must lie within the
+    plan's split items; decode checks it before any device work."""
+    nb, mb = 40, 36
+    _, info = segment_plan(0)
+    for bad in (-1, info.n_row_items + 1):
+        info.n_row_warp_items = bad
+        with pytest.raises(B.KVError) as e:
+            B.paged_decode_attn(FAKE, FAKE, FAKE, 4096, FAKE, FAKE, FAKE, 1, nb,
+                                mb, 64, 8, 128, 0.088, FAKE, FAKE, info,
+                                0x100000, info.workspace_bytes)
+        assert e.value.code == B.KV_ERR_INVALID_ARG
+        assert "n_row_warp_items" in str(e.value)   # this check, no other
+
+
 def test_e4m3_metadata_pool_replays_like_bf16():
     """The allocator does not depend on the element type."""
     from paged_kv_cache_attn_gb300 import harness as H
