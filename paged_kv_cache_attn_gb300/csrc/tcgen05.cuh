@@ -25,18 +25,8 @@ __host__ __device__ constexpr uint32_t idesc(int M, int N, bool b_mn) {
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b,
-                                     uint32_t id, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
-          tmem_d),
-      "l"(a), "l"(b), "r"(id), "r"(accumulate)
-      : "memory");
-}
-
-// Same with A read from tensor memory (16-bit A: two elements per column).
+// D (+)= A B, kind::f16, with A read from tensor memory (16-bit A: two
+// elements per column) and B from a shared-memory descriptor.
 __device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a,
                                         uint64_t b, uint32_t id,
                                         uint32_t accumulate) {
@@ -62,18 +52,6 @@ __device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster."
       "multicast::cluster.b64 [%0], %1;" ::"r"(bar),
       "h"(mask)
-      : "memory");
-}
-
-// 2-D TMA load written to the same offset in every CTA of `mask`, completing
-// on the mbarrier at `bar` in each of them.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* tm,
-                                               int x, int y, uint32_t bar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::"
-      "bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(tm), "r"(x), "r"(y), "r"(bar), "h"(mask)
       : "memory");
 }
 
