@@ -113,19 +113,25 @@ def unique_kv_bytes(tables, seq_lens, Hkv, d, elem=2, record=0):
             len(valid) * Hkv * record)
 
 
-def item_bytes(plan, info, Hkv, d, seq_lens, which, elem=2, record=0):
-    """Algorithmic KV bytes one launch of a kernel reads: for each of its work
-    items, the valid tokens of its block range x 2 (K, V) x d x elem bytes,
-    plus `record` bytes per block of the range (e4m3 scale records).  The
-    two CTAs of a tile-kernel cluster share one read of their common range
-    (TMA multicast), so a pair counts once."""
+def plan_items(plan, info, which):
+    """The work items of one kernel in a plan (int32 [n][8]: first branch,
+    kv-head, first row, rows, block range, partial-row base, masked)."""
     off = 16 if which == "row" else 16 + 8 * info.n_row_items
     n = info.n_row_items if which == "row" else info.n_tile_items
-    items = plan[off:off + 8 * n].reshape(-1, 8)
-    if which == "tile" and info.tile_cluster > 1:
-        items = items[::info.tile_cluster]
+    return plan[off:off + 8 * n].reshape(-1, 8)
+
+
+def item_bytes(plan, info, Hkv, d, seq_lens, which, elem=2, record=0,
+               segments_only=False):
+    """Algorithmic KV bytes one launch of a kernel reads: for each of its work
+    items, the valid tokens of its block range x 2 (K, V) x d x elem bytes,
+    plus `record` bytes per block of the range (e4m3 scale records).  With
+    segments_only, only the items over shared-prefix segments (masked == 0)
+    count."""
     tot = blocks = 0
-    for b0, g, row0, nr, lo, hi, pb, masked in items:
+    for b0, g, row0, nr, lo, hi, pb, masked in plan_items(plan, info, which):
+        if segments_only and masked:
+            continue
         toks = (hi - lo) * 16
         if masked:
             toks = min(toks, int(seq_lens[b0]) - 16 * lo)
@@ -510,16 +516,13 @@ def run_ours(args):
                                       bt.seq_lens, k) for k in ("row", "tile"))
         bytes_unshared = item_bytes(bu.plan, bu.info, w.Hkv, w.d, bu.seq_lens,
                                     "row")
+        # Prefix bytes: each branch re-reading every segment it is in,
+        # against what the shared plan's segment items read.
         kvb = 2 * w.d * 2 * w.Hkv * 16  # bytes per block, all kv-heads
         pref_unshared = int(sum(int(g[1]) * int(g[3]) for g in bt.groups)) * kvb
-        pref_shared = 0
-        for g in bt.groups:
-            rows = int(g[1]) * (w.Hq // w.Hkv)
-            if rows >= 65 and w.d == 128:        # tcgen05 tiles, paired
-                loads = -(-rows // (128 * bt.info.tile_cluster))
-            else:                                 # 16-row split items
-                loads = -(-rows // 16)
-            pref_shared += loads * int(g[3]) * kvb
+        pref_shared = sum(item_bytes(bt.plan, bt.info, w.Hkv, w.d, bt.seq_lens,
+                                     k, segments_only=True)
+                          for k in ("row", "tile"))
         sharing = {
             "ms_per_step_shared": round(ms_step, 5),
             "ms_per_step_per_branch_reread": round(ms_u, 5),

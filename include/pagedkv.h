@@ -381,9 +381,7 @@ typedef struct kv_decode_plan_info {
   int32_t n_tile_items;    /* 128-row work items of the tcgen05 kernel */
   int32_t n_merge_rows;    /* nb (one merge per branch and kv-head) */
   int32_t chunk_blocks;    /* blocks per split-KV item */
-  int32_t tile_cluster;    /* CTAs per cluster of the tcgen05 kernel (1 or 2):
-                              with 2, the two 128-row tiles of one segment
-                              share every K/V load (TMA multicast) */
+  int32_t reserved2;       /* 0 */
   int32_t flags;           /* the KV_PLAN_* flags the plan was made with */
   int32_t n_row_warp_items; /* the last n_row_warp_items of the split-KV
                                items are short (at most 16 blocks): the bf16

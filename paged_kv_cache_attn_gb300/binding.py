@@ -63,7 +63,7 @@ class kv_decode_plan_info(C.Structure):
     _fields_ = [("plan_ints", C.c_int64), ("workspace_bytes", C.c_int64),
                 ("partial_rows", C.c_int64), ("n_row_items", C.c_int32),
                 ("n_tile_items", C.c_int32), ("n_merge_rows", C.c_int32),
-                ("chunk_blocks", C.c_int32), ("tile_cluster", C.c_int32),
+                ("chunk_blocks", C.c_int32), ("reserved2", C.c_int32),
                 ("flags", C.c_int32), ("n_row_warp_items", C.c_int32),
                 ("reserved", C.c_int32)]
 

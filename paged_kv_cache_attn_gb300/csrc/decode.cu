@@ -569,8 +569,7 @@ cudaError_t launch_tile_e4m3(const SplitParams& sp, const WorkItem* items,
 // Tensor-core (tcgen05) kernel for 128-row tiles; defined in decode_tc.cu.
 cudaError_t launch_tile_items(const CUtensorMap& tk, const CUtensorMap& tv,
                               const SplitParams& sp, const WorkItem* items,
-                              int n_items, int d, int cluster,
-                              cudaStream_t stream);
+                              int n_items, int d, cudaStream_t stream);
 
 // Second stream (and fork / join events) per device: the tensor-core tile
 // pass runs beside the split-KV pass so that the tile kernel's tensor work
@@ -665,8 +664,8 @@ static kv_status decode_impl(
     return fail(KV_ERR_INVALID_ARG, e4m3 ? "an e4m3 step needs a plan made "
                                            "with KV_PLAN_KV_E4M3"
                                          : "plan was made for an e4m3 pool");
-  if (e4m3 && info->n_tile_items != 0 && (d != 128 || info->tile_cluster != 1))
-    return fail(KV_ERR_INVALID_ARG, "e4m3 tiles need head_dim 128, no clusters");
+  if (info->n_tile_items != 0 && d != 128)
+    return fail(KV_ERR_INVALID_ARG, "tensor-core tiles need head_dim 128");
   if ((uintptr_t)workspace & 255)
     return fail(KV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   if (!std::isfinite(scale) || !(scale > 0.f))
@@ -751,8 +750,7 @@ static kv_status decode_impl(
     e = e4m3 ? pkv::launch_tile_e4m3(sp, titems, info->n_tile_items, k_pool,
                                      v_pool, kv_scales, ts)
              : pkv::launch_tile_items(tk_tiles, tv_tiles, sp, titems,
-                                      info->n_tile_items, d,
-                                      info->tile_cluster, ts);
+                                      info->n_tile_items, d, ts);
     pkv::mark(1, ts);
     if (e != cudaSuccess)
       return fail(KV_ERR_CUDA, "tile kernel: %s", cudaGetErrorString(e));

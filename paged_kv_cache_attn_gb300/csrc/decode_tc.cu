@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tile_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
                        const SplitParams p, const WorkItem* items,
-                       int oob_tile, int cluster) {
+                       int oob_tile) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) Bars bars;
   __shared__ uint32_t tmem_base_sh;
@@ -84,16 +84,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sK = base;                        // K ring
   const uint32_t sV = sK + kNS * kKV;              // V ring
   WorkItem it = items[blockIdx.x];
-  // In a cluster the partner of an odd last tile has no rows (nrows == 0).
-  // A malformed item is recorded and runs with no rows and no tiles; it
-  // still takes part in the cluster barriers so that its partner can finish.
-  const bool good =
-      (it.nrows == 0 && cluster > 1 && it.row0 >= 0 && it.g >= 0 &&
-       it.g < p.Hkv && it.branch0 >= 0 && it.branch0 < p.nb &&
-       it.blk_begin >= 0 && it.blk_begin < it.blk_end &&
-       it.blk_end <= p.max_blocks) ||
-      item_ok(it, p, 128);
-  if (!good) {
+  // A malformed item is recorded and runs with no rows and no tiles.
+  if (!item_ok(it, p, 128)) {
     if (threadIdx.x == 0)
       record_status(p.status, KV_ERR_DEVICE, -1 - (int)blockIdx.x);
     it.nrows = 0;
@@ -102,16 +94,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int nblk = it.blk_end - it.blk_begin;
   const int ntile = (nblk + kTB - 1) / kTB;
-  const uint32_t crank = cluster > 1 ? cluster_rank() : 0;
-  const uint16_t cmask = (uint16_t)((1u << cluster) - 1u);
   const int32_t* table = p.tables + (int64_t)it.branch0 * p.max_blocks;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNS; ++s) {
       mbar_init(smem_u32(&bars.k_full[s]), 2);   // two K producer warps
-      mbar_init(smem_u32(&bars.k_empty[s]), cluster);  // every CTA's MMA
+      mbar_init(smem_u32(&bars.k_empty[s]), 1);  // the MMA issuer's commit
       mbar_init(smem_u32(&bars.v_full[s]), 2);   // two V producer warps
-      mbar_init(smem_u32(&bars.v_empty[s]), cluster);
+      mbar_init(smem_u32(&bars.v_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&bars.s_full[b]), 1);
     mbar_init(smem_u32(&bars.p_full), 4);
@@ -135,12 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmV);
   }
   fence_before_sync();
-  // The partner's barriers must be initialised before any multicast load or
-  // remote arrive reaches them.
-  if (cluster > 1)
-    cluster_sync();
-  else
-    __syncthreads();
+  __syncthreads();
   fence_after_sync();
   // Q tile into TMEM columns kColQ.. (lane r = row r = (branch, q-head) of
   // the segment; column c holds elements 2c and 2c + 1).
@@ -181,9 +166,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 5) {
     // ---- TMA producers: warps 5 / 6 = K blocks 0-3 / 4-7 of a tile, warps
     // 7 / 8 = V.  One box is a whole (block, kv-head) tile of 4 KB; a warp
-    // issues its blocks from lanes 0-3 (0-1 in a pair, which splits them) in
-    // one instruction.  A K stage frees as soon as its QK product is done, a
-    // V stage after its PV product; K and V producers run independently.
+    // issues its blocks from lanes 0-3 in one instruction.  A K stage frees
+    // as soon as its QK product is done, a V stage after its PV product; K
+    // and V producers run independently.
     // Block-table entries are staged in shared memory, kTblWin at a time,
     // with coalesced loads.
     const int pw = warp - 5;
@@ -216,8 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      if (lane < kTB / 2 / cluster) {
-        const int bi = half * (kTB / 2) + lane * cluster + (int)crank;
+      if (lane < kTB / 2) {
+        const int bi = half * (kTB / 2) + lane;
         const int rel = j * kTB + bi;
         int y = oob_tile;  // zero fill past the range
         if (it.blk_begin + rel < it.blk_end) {
@@ -227,11 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           else if (pw == 0)
             record_status(p.status, KV_ERR_DEVICE, phys);
         }
-        const uint32_t dst = ring + s * kKV + bi * kBlk;
-        if (cluster > 1)
-          tma_load_5d_mc(dst, tm, y, smem_u32(&full[s]), cmask);
-        else
-          tma_load_5d(dst, tm, y, smem_u32(&full[s]));
+        tma_load_5d(ring + s * kKV + bi * kBlk, tm, y, smem_u32(&full[s]));
       }
       __syncwarp();
       issued = j + 1;
@@ -263,10 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ts(tmem + kColO, tmem + (jp & 1) * kT + kt * 8, bd, id_pv,
                   (jp > 0 || kt > 0) ? 1u : 0u);
         }
-        if (cluster > 1)
-          umma_commit_mc(smem_u32(&bars.v_empty[s]), cmask);
-        else
-          umma_commit(smem_u32(&bars.v_empty[s]));
+        umma_commit(smem_u32(&bars.v_empty[s]));
         umma_commit(smem_u32(&bars.pv_done));
         return true;
       };
@@ -285,10 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ts(tmem + b * kT, tmem + kColQ + kk * 8, bd, id_qk,
                   kk > 0 ? 1u : 0u);
         }
-        if (cluster > 1)
-          umma_commit_mc(smem_u32(&bars.k_empty[s]), cmask);
-        else
-          umma_commit(smem_u32(&bars.k_empty[s]));
+        umma_commit(smem_u32(&bars.k_empty[s]));
         umma_commit(smem_u32(&bars.s_full[b]));
         if (j >= 1) ok = pv(j - 1);
       }
@@ -429,17 +404,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         "r"(kTmemCols)
         : "memory");
   }
-  // No CTA leaves while its partner may still write into its shared memory
-  // or arrive on its barriers.
-  if (cluster > 1) cluster_sync();
 }
 
 }  // namespace tc
 
 cudaError_t launch_tile_items(const CUtensorMap& tk, const CUtensorMap& tv,
                               const SplitParams& sp, const WorkItem* items,
-                              int n_items, int d, int cluster,
-                              cudaStream_t stream) {
+                              int n_items, int d, cudaStream_t stream) {
   if (d != 128) return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
@@ -452,22 +423,9 @@ cudaError_t launch_tile_items(const CUtensorMap& tk, const CUtensorMap& tv,
   // A (block, head) index past the end of the pool: TMA fills with zeros.
   if ((int64_t)sp.num_blocks * sp.Hkv > INT32_MAX - 1) return cudaErrorInvalidValue;
   const int oob_tile = (int)((int64_t)sp.num_blocks * sp.Hkv);
-  if (cluster < 1 || cluster > 2 || n_items % cluster != 0)
-    return cudaErrorInvalidValue;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_items);
-  cfg.blockDim = dim3(tc::kThreads);
-  cfg.dynamicSmemBytes = tc::kSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc::tile_decode_kernel, tk, tv, sp, items,
-                            oob_tile, cluster);
+  tc::tile_decode_kernel<<<n_items, tc::kThreads, tc::kSmem, stream>>>(
+      tk, tv, sp, items, oob_tile);
+  return cudaGetLastError();
 }
 
 }  // namespace pkv

@@ -144,15 +144,6 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   std::stable_sort(units.begin(), units.end(), [](const Unit& x, const Unit& y) {
     return (x.blk_end - x.blk_begin) > (y.blk_end - y.blk_begin);
   });
-  // Tile units with more than one 128-row tile run as clusters of two CTAs
-  // (one per tile of the same segment, kv-head and block range) that share
-  // every K/V load; an odd last tile is paired with a row-less partner.
-  // (The e4m3 tile kernel runs single CTAs.)
-  int32_t tile_cluster = 1;
-  for (const Unit& u : units)
-    if (u.tile && u.rows > pkv::kTileRows && !(flags & KV_PLAN_KV_E4M3))
-      tile_cluster = 2;
-
   std::vector<pkv::WorkItem> row_items, tile_items;
   struct Tagged { int32_t branch; pkv::MergeEntry e; };
   std::vector<Tagged> merge_flat;
@@ -164,9 +155,7 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
       const int rows_per = u.tile ? pkv::kTileRows : pkv::kRowTile;
       const int64_t nch =
           ceil_div(u.blk_end - u.blk_begin, u.tile ? chunk_tile : chunk_rows);
-      const int64_t tiles = u.tile && tile_cluster == 2
-                                ? 2 * ceil_div(u.rows, 2 * rows_per)
-                                : ceil_div(u.rows, rows_per);
+      const int64_t tiles = ceil_div(u.rows, rows_per);
       (u.tile ? n_tile : n_row) += nch * tiles * Hkv;
       n_merge += nch * tiles * (rows_per / G + 2);
     }
@@ -184,33 +173,6 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
       // Even split of the range into nch pieces.
       const int32_t lo = u.blk_begin + (int32_t)((int64_t)len * c / nch);
       const int32_t hi = u.blk_begin + (int32_t)((int64_t)len * (c + 1) / nch);
-      if (u.tile && tile_cluster == 2) {
-        for (int32_t row0 = 0; row0 < u.rows; row0 += 2 * rows_per) {
-          int32_t nr[2], base[2];
-          for (int m = 0; m < 2; ++m) {
-            nr[m] = std::max(0, std::min(rows_per, u.rows - row0 - m * rows_per));
-            base[m] = (int32_t)prow;
-            prow += (int64_t)nr[m] * Hkv;
-          }
-          if (prow > INT32_MAX)
-            return fail(KV_ERR_INVALID_ARG, "step too large for one plan");
-          for (int32_t g = 0; g < Hkv; ++g)
-            for (int m = 0; m < 2; ++m)
-              tile_items.push_back({u.branch0, g, row0 + m * rows_per, nr[m],
-                                    lo, hi, base[m] + g * nr[m], 0});
-          for (int m = 0; m < 2; ++m) {
-            const int32_t r0 = row0 + m * rows_per, r1 = r0 + nr[m];
-            for (int32_t pb = r0 / G; nr[m] > 0 && pb * G < r1; ++pb) {
-              const int32_t a = std::max(r0, pb * G);
-              const int32_t e = std::min(r1, pb * G + G);
-              merge_flat.push_back(
-                  {u.branch0 + pb,
-                   {base[m] + (a - r0), nr[m], a - pb * G, e - pb * G}});
-            }
-          }
-        }
-        continue;
-      }
       for (int32_t row0 = 0; row0 < u.rows; row0 += rows_per) {
         const int32_t nrows = std::min(rows_per, u.rows - row0);
         const int64_t base0 = prow;
@@ -259,7 +221,7 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   info->n_tile_items = (int32_t)tile_items.size();
   info->n_merge_rows = nb;
   info->chunk_blocks = chunk_rows;
-  info->tile_cluster = tile_cluster;
+  info->reserved2 = 0;
   info->flags = flags;
   if (!plan) return KV_OK;
   if (plan_cap < total)
@@ -281,7 +243,7 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   h[pkv::H_OFF_CSR_ENT] = (int32_t)off_ent;
   h[pkv::H_PARTIAL_ROWS] = (int32_t)prow;
   h[pkv::H_CHUNK] = chunk_rows;
-  h[pkv::H_FLAGS] = flags | (tile_cluster << 16);
+  h[pkv::H_FLAGS] = flags;
   h[pkv::H_TOTAL] = (int32_t)total;
   std::memcpy(h + off_row, row_items.data(), row_items.size() * 32);
   std::memcpy(h + off_tile, tile_items.data(), tile_items.size() * 32);

@@ -1,4 +1,4 @@
-// tcgen05 / TMEM / cluster helpers shared by the tensor-core decode kernels.
+// tcgen05 / TMEM / TMA helpers shared by the tensor-core decode kernels.
 // Inline PTX for sm_103a.
 #pragma once
 
@@ -45,16 +45,6 @@ __host__ __device__ constexpr uint32_t idesc_k0(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// Arrive on the mbarrier at this offset in every CTA of `mask` once this
-// thread's earlier MMAs are done.
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster."
-      "multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
-
 // 5-D TMA load (coordinates x0..x4) into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* tm,
                                             int x4, uint32_t bar) {
@@ -63,29 +53,6 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* tm,
       "bytes [%0], [%1, {%2, %2, %2, %2, %3}], [%4];" ::"r"(dst),
       "l"(tm), "r"(0), "r"(x4), "r"(bar)
       : "memory");
-}
-
-// The same written to the same offset in every CTA of `mask`.
-__device__ __forceinline__ void tma_load_5d_mc(uint32_t dst, const CUtensorMap* tm,
-                                               int x4, uint32_t bar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::"
-      "bytes.multicast::cluster [%0], [%1, {%2, %2, %2, %2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(tm), "r"(0), "r"(x4), "r"(bar), "h"(mask)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Every thread of every CTA of the cluster.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void umma_commit(uint32_t bar) {

@@ -162,7 +162,7 @@ def test_e4m3_decode_matches_oracle(name, flags):
     assert cache.decode_ids == ref.decode_ids
     q = w.queries(len(cache.decode_ids))
     gpu, bt = run_decode(cache, q, flags)
-    assert bt.info.flags & B.KV_PLAN_KV_E4M3 and bt.info.tile_cluster == 1
+    assert bt.info.flags & B.KV_PLAN_KV_E4M3
     if flags or w.d != 128:
         assert bt.info.n_tile_items == 0
     assert_close(gpu, rp.decode_all_from_pool(ref, q, w.scale), name)

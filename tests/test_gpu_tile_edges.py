@@ -4,7 +4,7 @@ three tiles (the depth of the bf16 kernel's K/V rings and of the e4m3
 kernel's K code ring), three tiles and a block, eight tiles and a block, and
 a long segment (40 tiles and a ragged tail) that wraps every ring many times.
 Each tree has 20 branches x 8 q-heads per kv-head = 160 rows, so a segment
-is two 128-row tiles (a cluster pair for bf16, the second tile ragged); the
+is two 128-row tiles (the second one ragged); the
 branches' own suffixes go to the split-KV pass.  The plan is made for one SM
 (the split sizes do not change the result), so that each tile item covers
 its whole segment (up to 256 blocks) instead of a short chunk of it.

@@ -73,13 +73,12 @@ def segment_plan(flags):
     return B.paged_decode_plan(nb, 64, 8, 128, mb, lens, groups, 152, flags)
 
 
-def test_plan_records_its_flags_and_keeps_e4m3_tiles_unpaired():
+def test_plan_records_its_flags():
     _, bf = segment_plan(0)
     _, e8 = segment_plan(B.KV_PLAN_KV_E4M3)
-    assert bf.flags == 0 and bf.tile_cluster == 2      # bf16: pairs
-    assert e8.flags == B.KV_PLAN_KV_E4M3
-    assert e8.n_tile_items > 0 and e8.tile_cluster == 1
+    assert bf.flags == 0 and e8.flags == B.KV_PLAN_KV_E4M3
     # the same rows and blocks are covered either way: 3 tiles x 8 heads
+    assert e8.n_tile_items > 0 and e8.n_tile_items == bf.n_tile_items
     assert e8.n_tile_items == 3 * 8 * (e8.n_tile_items // 24)
     _, nt = segment_plan(B.KV_PLAN_KV_E4M3 | B.KV_PLAN_NO_TENSOR_CORES)
     assert nt.n_tile_items == 0

@@ -263,9 +263,7 @@ def test_plan_covers_every_token_once(name, flags):
     written = np.zeros(bt.info.partial_rows, dtype=int)
     for it in np.concatenate([rows, tiles]):
         b0, g, row0, nr, lo, hi, pbase, masked = [int(x) for x in it]
-        assert 0 <= lo < hi <= nblk[b0]
-        if nr == 0:          # row-less partner of a cluster pair
-            continue
+        assert 0 <= lo < hi <= nblk[b0] and nr >= 1
         written[pbase:pbase + nr] += 1
         for r in range(row0, row0 + nr):
             b, qr = b0 + r // G, r % G
@@ -282,7 +280,7 @@ def test_plan_covers_every_token_once(name, flags):
     row_owner = {}
     for it in np.concatenate([rows, tiles]):
         b0, g, row0, nr, lo, hi, pbase, masked = [int(x) for x in it]
-        for r in range(nr):  # (row-less partners own no rows)
+        for r in range(nr):
             row_owner[pbase + r] = (b0 + (row0 + r) // G, g, (row0 + r) % G,
                                     hi - lo)
     for b in range(nb):
@@ -321,18 +319,21 @@ def test_short_split_items_keep_their_order():
     assert sorted(base.tolist()) == sorted(set(base.tolist()))
 
 
-def test_multi_tile_segments_run_as_pairs():
-    # 40 branches x 8 q-heads = 320 rows: three 128-row tiles, paired with a
-    # row-less partner for the third; both CTAs of a pair read the same blocks.
+def test_multi_tile_segments_split_into_128_row_tiles():
+    # 40 branches x 8 q-heads = 320 rows: 128-row tiles of 128, 128 and 64
+    # rows, each over every block range and kv-head of the segment.
     w = W.fanout(n_roots=1, root_tokens=512, fan=40, min_suffix=1,
                  max_suffix=50, Hq=64, Hkv=8)
     bt = H.Cache(w, with_data=False).batch(num_sms=152)
-    assert bt.info.tile_cluster == 2 and bt.info.n_tile_items % 2 == 0
+    assert bt.info.reserved2 == 0
     rows, tiles, ptr, ent = decode_plan(bt.plan, bt.info, bt.nb, w.Hq, w.Hkv)
-    for a, b in zip(tiles[0::2], tiles[1::2]):
-        assert a[0] == b[0] and a[1] == b[1] and (a[4], a[5]) == (b[4], b[5])
-        assert b[2] == a[2] + 128
-    assert (tiles[:, 3] == 0).sum() == 8 * len({(t[4], t[5]) for t in tiles})
+    ranges = {(int(t[4]), int(t[5])) for t in tiles}
+    assert len(tiles) == 3 * 8 * len(ranges)
+    for lo, hi in ranges:
+        for g in range(8):
+            got = sorted((int(t[2]), int(t[3])) for t in tiles
+                         if (t[4], t[5]) == (lo, hi) and t[1] == g)
+            assert got == [(0, 128), (128, 128), (256, 64)]
 
 
 def test_plan_rejects_bad_input():
