@@ -112,3 +112,49 @@ def test_spilled_branch_is_guarded():
     B.kv_free(h, a)
     assert len(B.kv_get_free_stack(h)) == 16 and len(B.kv_get_host_free(h)) == 8
     B.kv_pool_destroy(h)
+
+
+class _LibOps:
+    """The host-tier scenario's operations on the library (metadata-only
+    pool of 10 blocks, ascending free order, 4 host slots)."""
+
+    def __init__(self):
+        self.h = B.kv_pool_create(10, 1, 1, 64)
+        B.kv_offload_attach(self.h, None, None, 4)
+
+    def create(self):
+        return B.kv_branch_create(self.h)
+
+    def append(self, i, n):
+        B.kv_append(self.h, i, n)
+
+    def fork(self, i):
+        return B.kv_fork_branch(self.h, i)
+
+    def spill(self, ids):
+        return B.kv_spill(self.h, ids)
+
+    def restore(self, ids):
+        return B.kv_restore(self.h, ids)
+
+    def free(self, i):
+        B.kv_free(self.h, i)
+
+    def table(self, i):
+        return B.kv_get_block_table(self.h, i)[0].tolist()
+
+    def free_stack(self):
+        return B.kv_get_free_stack(self.h).tolist()
+
+    def host_free(self):
+        return B.kv_get_host_free(self.h).tolist()
+
+    def ref(self):
+        return B.kv_get_refcounts(self.h, 10).tolist()
+
+
+def test_host_tier_hand_worked_scenario_on_the_library():
+    from test_oracle_allocator import HOST_TIER_WANT, _host_tier_scenario
+    ops = _LibOps()
+    assert _host_tier_scenario(ops) == HOST_TIER_WANT
+    B.kv_pool_destroy(ops.h)

@@ -175,3 +175,129 @@ def test_deep_tree_eviction_reaches_target():
     assert len(w.leaves()) == 243
     assert 243 - len(r.decode_ids) >= w.evict_target_leaves() == 73
     r.model.check_invariants()
+
+
+# ---- host tier ("Dismantling the Memory Wall", cross-tier offloading) -------
+
+def _host_tier_scenario(ops):
+    """A scenario worked by hand from the host-tier reading (blocks a branch
+    owns alone move to host slots in branch and table order; freed device
+    blocks and emptied host slots are pushed on their LIFO stacks as they are
+    freed; a spilled entry is -(slot + 2); a restore pops device blocks in
+    branch and table order).  `ops` supplies create / append / fork / spill /
+    restore / free and the state readers, so the same script runs on the
+    oracle's model and on the library."""
+    a = ops.create()
+    ops.append(a, 40)                 # blocks 0, 1, 2 (8 tokens in 2)
+    b = ops.fork(a)                   # COW block 3 <- copy of 2; shares 0, 1
+    ops.append(b, 20)                 # 8 more tokens into 3, then block 4
+    got = {"b0": ops.table(b)}
+    got["spill_b"] = ops.spill([b])   # 3 -> slot 0, 4 -> slot 1
+    got["b1"] = ops.table(b)
+    got["free1"] = ops.free_stack()
+    got["host1"] = ops.host_free()
+    got["spill_a"] = ops.spill([a])   # only 2 is a's alone -> slot 2
+    got["a1"] = ops.table(a)
+    got["restore"] = ops.restore([b, a])
+    got["a2"], got["b2"] = ops.table(a), ops.table(b)
+    got["free2"] = ops.free_stack()
+    got["host2"] = ops.host_free()
+    ops.spill([a])                    # a's block 3 -> slot 2 (top of host)
+    got["a3"] = ops.table(a)
+    ops.free(a)                       # 0, 1 drop to refcount 1; slot 2 back
+    got["ref"] = ops.ref()
+    got["free3"] = ops.free_stack()
+    got["host3"] = ops.host_free()
+    return got
+
+
+HOST_TIER_WANT = {
+    "b0": [0, 1, 3, 4],
+    "spill_b": 2,
+    "b1": [0, 1, -2, -3],
+    "free1": [4, 3, 5, 6, 7, 8, 9],
+    "host1": [2, 3],
+    "spill_a": 1,
+    "a1": [0, 1, -4],
+    "restore": 3,
+    # b's slot 0 -> block 2 (top of the device stack), slot 1 -> block 4;
+    # a's slot 2 -> block 3; each slot pushed back as it empties.
+    "b2": [0, 1, 2, 4],
+    "a2": [0, 1, 3],
+    "free2": [5, 6, 7, 8, 9],
+    "host2": [2, 1, 0, 3],
+    "a3": [0, 1, -4],
+    "ref": [1, 1, 1, 0, 1, 0, 0, 0, 0, 0],
+    "free3": [3, 5, 6, 7, 8, 9],
+    "host3": [2, 1, 0, 3],
+}
+
+
+class _ModelOps:
+    def __init__(self):
+        self.m = al.PoolModel(10, 16)
+        self.m.attach_host(4)
+
+    def create(self):
+        return self.m.create()
+
+    def append(self, i, n):
+        self.m.append(i, n)
+
+    def fork(self, i):
+        return self.m.fork(i)[0]
+
+    def spill(self, ids):
+        return len(self.m.spill(ids))
+
+    def restore(self, ids):
+        return len(self.m.restore(ids))
+
+    def free(self, i):
+        self.m.free_node(i)
+
+    def table(self, i):
+        return list(self.m.nodes[i].table)
+
+    def free_stack(self):
+        return self.m.free_stack()
+
+    def host_free(self):
+        return self.m.host_free_stack()
+
+    def ref(self):
+        return list(self.m.ref)
+
+
+def test_host_tier_hand_worked_scenario():
+    got = _host_tier_scenario(_ModelOps())
+    assert got == HOST_TIER_WANT
+
+
+def test_host_tier_pairs_name_the_copies():
+    """The copies a spill or restore returns: (device block, host slot) in
+    branch and table order, then (host slot, device block)."""
+    m = al.PoolModel(10, 16)
+    m.attach_host(4)
+    a = m.create()
+    m.append(a, 40)
+    b = m.fork(a)[0]
+    m.append(b, 20)
+    assert m.spill([b]) == [(3, 0), (4, 1)]
+    assert m.spill([a]) == [(2, 2)]
+    assert m.restore([b, a]) == [(0, 2), (1, 4), (2, 3)]
+    m.check_invariants()
+
+
+def test_host_tier_refusals_leave_the_model_unchanged():
+    m = al.PoolModel(4, 16)
+    m.attach_host(1)
+    a = m.create()
+    m.append(a, 40)                    # three blocks of a's own
+    before = (list(m.nodes[a].table), m.free_stack(), m.host_free_stack())
+    with pytest.raises(al.OutOfBlocks):
+        m.spill([a])                   # three blocks, one host slot
+    assert (list(m.nodes[a].table), m.free_stack(),
+            m.host_free_stack()) == before
+    with pytest.raises(ValueError):
+        m.restore([a, a])
