@@ -509,9 +509,10 @@ kv_status paged_decode_append_attn_e4m3(
  * first call on a device looks up the array's device address (with that
  * device current) and should come before any stream capture.  All calls share
  * the array and it keeps the last call's contents; each call clears the part
- * that must start at zero; calls whose work overlaps on the GPU race.  Kernel
- * status recorded in this scratch is not readable by kv_check_device_status.
- * Calls no cudaMalloc, cudaFree or other allocating routine. */
+ * that must start at zero; calls whose work overlaps on the GPU race.  A bad
+ * block id or a timed-out wait is recorded in the status word at the start of
+ * the array; kv_check_noalloc_status reads it.  Calls no cudaMalloc, cudaFree
+ * or other allocating routine. */
 kv_status paged_decode_attn_noalloc(
     const void* q, const void* k_pool, const void* v_pool, int64_t num_blocks,
     const int32_t* block_tables, const int32_t* seq_lens,
@@ -519,6 +520,17 @@ kv_status paged_decode_attn_noalloc(
     int32_t max_blocks, int32_t Hq, int32_t Hkv, int32_t head_dim,
     int32_t block_size, float scale, void* out, const int32_t* plan,
     const kv_decode_plan_info* info, void* stream);
+
+/* The status word of paged_decode_attn_noalloc's built-in scratch on the
+ * current device, read (synchronising `stream`) and cleared, as
+ * kv_check_device_status does for a caller workspace: *out_code 0,
+ * KV_ERR_DEVICE or KV_ERR_TIMEOUT; *out_detail (nullable) the first bad value
+ * recorded.  Like the entry point it serves, it has no counterpart in the
+ * pages and allocates nothing.  Each paged_decode_attn_noalloc call clears
+ * the word when it starts, so read it after the call whose errors are
+ * wanted and before the next one.  Errors: INVALID_ARG, CUDA. */
+kv_status kv_check_noalloc_status(void* stream, int32_t* out_code,
+                                  int32_t* out_detail);
 
 /* Read (synchronising `stream`) and clear the status word of a workspace used
  * by paged_decode_attn.  *out_code: 0, KV_ERR_DEVICE or KV_ERR_TIMEOUT;

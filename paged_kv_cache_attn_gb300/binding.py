@@ -136,6 +136,8 @@ _SIGS = {
                                               _vp, _vp,
                                               C.POINTER(kv_decode_plan_info),
                                               _vp]),
+    "kv_check_noalloc_status": (C.c_int32, [_vp, C.POINTER(C.c_int32),
+                                            C.POINTER(C.c_int32)]),
     "paged_decode_attn_e4m3": (C.c_int32, [_vp, _vp, _vp, _vp, C.c_int64, _vp,
                                            _vp, _vp, C.c_int32, C.c_int32,
                                            C.c_int32, C.c_int32, C.c_int32,
@@ -491,6 +493,16 @@ def paged_decode_attn_noalloc(q, k_pool, v_pool, num_blocks, block_tables,
         _ptr(seq_lens), _ptr(prefix_groups), n_groups, nb, max_blocks, Hq, Hkv,
         head_dim, block_size, scale, _ptr(out), _ptr(plan), C.byref(info),
         _stream(stream)))
+
+
+def kv_check_noalloc_status(stream=None):
+    """(code, detail) of the built-in scratch's status word on the current
+    device, read and cleared."""
+    code = C.c_int32()
+    detail = C.c_int32()
+    _check(_lib.kv_check_noalloc_status(_stream(stream), C.byref(code),
+                                        C.byref(detail)))
+    return code.value, detail.value
 
 
 def kv_selftest_timeout(workspace, wait_cycles, stream=None):

@@ -19,7 +19,8 @@
 // array and it keeps the last call's contents: the only part that must start
 // at zero (the status word) is cleared by every call, and calls whose work
 // overlaps on the GPU race on the array.  No cudaMalloc, cudaFree or other
-// allocating routine is called.
+// allocating routine is called.  kv_check_noalloc_status reads the status
+// word (a bad block id or a timed-out wait) that the kernels record there.
 
 #include <cuda_runtime.h>
 
@@ -87,4 +88,13 @@ extern "C" kv_status paged_decode_attn_noalloc(
                            seq_lens, prefix_groups, n_groups, nb, max_blocks,
                            Hq, Hkv, head_dim, block_size, scale, out, plan,
                            info, scratch, pkv::kNoAllocScratchBytes, stream);
+}
+
+extern "C" kv_status kv_check_noalloc_status(void* stream, int32_t* out_code,
+                                             int32_t* out_detail) {
+  pkv::clear_error();
+  if (!out_code) return pkv::fail(KV_ERR_INVALID_ARG, "null out_code");
+  void* scratch = nullptr;
+  if (kv_status s = pkv::scratch_address(&scratch)) return s;
+  return kv_check_device_status(scratch, stream, out_code, out_detail);
 }
