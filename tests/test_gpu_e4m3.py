@@ -343,32 +343,22 @@ def test_e4m3_spill_restore_round_trip():
     cache.close()
 
 
-def test_e4m3_full_size_sampled_rows():
-    """The benchmarked long-context workload in e4m3: sampled rows against the
-    oracle quantising each sampled branch from its own token sequence."""
-    w = W.CONFIGS["long_context"]()
+@pytest.mark.parametrize("name", ["independent", "fanout", "deep_tree",
+                                  "long_context"])
+def test_e4m3_full_size_every_row(name):
+    """The benchmarked workloads over e4m3 pools at full size: every output
+    element against the oracle quantising each branch from its own token
+    sequence (in worker processes spawned after the GPU step)."""
+    import _oracle_pool
+    w = W.CONFIGS[name]()
     cache = H.Cache(w, kv_dtype="e4m3")
-    ref = rp.replay(w, with_data=False)
-    assert cache.decode_ids == ref.decode_ids
+    assert cache.decode_ids == _oracle_pool.decode_ids(name)
     nb = len(cache.decode_ids)
     q = w.queries(nb)
     gpu, bt = run_decode(cache, q)
-    rng = np.random.default_rng(5)
-    rows = sorted(set([0, nb - 1] + rng.choice(nb, 3, replace=False).tolist()))
-    G = w.Hq // w.Hkv
-    for b in rows:
-        nid = cache.decode_ids[b]
-        kb, vb = ref.branch_kv(nid)
-        lens = [hi - lo for _s, lo, hi in ref.logical[nid]]
-        kq = fp8.quantize_sequence(lens, kb)[0]
-        vq = fp8.quantize_sequence(lens, vb)[0]
-        for g in range(w.Hkv):
-            qr = att.bf16_to_f64(q[b, g * G:(g + 1) * G])
-            assert_close(gpu[b, g * G:(g + 1) * G],
-                         att.attention(qr, kq[:, g], vq[:, g], w.scale),
-                         f"row {b} head group {g}")
-    assert np.isfinite(gpu).all() and np.abs(gpu).max() < 8
     cache.close()
+    want = _oracle_pool.all_rows(name, q, "e4m3")
+    assert_close(gpu, want, f"{name} e4m3 ({nb} branches, every row)")
 
 
 def test_e4m3_stale_shared_memory_does_not_leak():
