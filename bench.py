@@ -61,6 +61,13 @@ def parse():
     ap.add_argument("--fused-steps", type=int, default=30)
     ap.add_argument("--offload-branches", type=int, default=32)
     ap.add_argument("--e4m3-steps", type=int, default=300)
+    ap.add_argument("--profile-step", choices=["shared", "reread"],
+                    help="run only `--steps` decode steps of --workload (plan "
+                         "with its shared-prefix segments, or with every "
+                         "branch re-reading its whole table) and exit: the "
+                         "command ncu captures for the sharing figures")
+    ap.add_argument("--per-config-steps", type=int, default=200,
+                    help="steps for each of the other configurations (0: skip)")
     return ap.parse_args()
 
 
@@ -207,6 +214,30 @@ def traffic_per_launch(kernel, workload):
     return d["dram_bytes_per_launch"] if sha == d["source_sha"] else None
 
 
+def measured_sharing(workload):
+    """Prefix bytes moved, re-read arm / shared arm, from the committed ncu
+    summary (profiles/ncu_sharing.json) if it was taken on the current kernel
+    sources; a workload is looked up under its own name or its quarter-size
+    profiling case."""
+    p = os.path.join(ROOT, "profiles", "ncu_sharing.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    for src, sha in d["sources"].items():
+        f = os.path.join(ROOT, "paged_kv_cache_attn_gb300", "csrc", src)
+        if hashlib.sha256(open(f, "rb").read()).hexdigest()[:16] != sha:
+            return None
+    e = d.get(workload) or d.get(workload + "_quarter")
+    if not e:
+        return None
+    return {"case": workload if workload in d else workload + "_quarter",
+            "branch_sharing_factor": e["branch_sharing_factor"],
+            "prefix_l2_requests_factor": e["prefix_l2_tex_factor"],
+            "prefix_l2_sectors_factor": e["prefix_l2_factor"],
+            "prefix_dram_factor": e["prefix_dram_factor"],
+            "source": "profiles/ncu_sharing.json"}
+
+
 # ---- the oracle as the CPU baseline ----------------------------------------------
 
 def prepare_sample(w, max_rows):
@@ -246,13 +277,13 @@ def run_units(w, sample, units, cores, ex):
     return sum(f.result() for f in [ex.submit(part, p) for p in parts])
 
 
-def cpu_baseline(w, budget_s=12.0):
+def cpu_baseline(w, budget_s=12.0, threads=None):
     """Oracle throughput on host threads over a bounded sample of the batch:
     passes over the sampled (branch, kv-head) units until ~budget_s of wall
-    time (at least one pass)."""
+    time (at least one pass).  threads: how many (default: every core)."""
     sample, nb = prepare_sample(w, 24)
     units = [(i, g) for i in range(len(sample)) for g in range(w.Hkv)]
-    cores = min(host_cores(), len(units))
+    cores = min(threads or host_cores(), len(units))
     done, byts, t0 = 0, 0, time.perf_counter()
     with cf.ThreadPoolExecutor(max_workers=cores) as ex:
         while done < len(units) or time.perf_counter() - t0 < budget_s:
@@ -270,6 +301,153 @@ def cpu_baseline(w, budget_s=12.0):
 
 
 # ---- our arm ------------------------------------------------------------------------
+
+KERNEL_NAMES = {"splitkv_mma": "splitkv_decode_kernel",
+                "tile_tcgen05": "tile_decode_kernel"}
+
+
+def time_steps(bt, q, out, K, warmup, flush=None, before=None):
+    """Time K decode steps after `warmup` untimed ones.  Returns (ms per step,
+    per-kernel ms, per-step kernel events).  Every step records, on the
+    launching streams, the library's per-kernel events.  With `flush` (two
+    device buffers, each larger than L2) the first is rewritten and the
+    second read before each step -- the write evicts the step's KV from L2,
+    the read then evicts the written lines, so that the step neither finds
+    the previous one's KV in L2 nor pays for the flush's write-backs -- and
+    each step is timed by its own pair of events.  `before` (optional) runs right before the
+    timed steps, after the warm-up (the ranks' barrier)."""
+    import torch
+    from paged_kv_cache_attn_gb300 import binding as B
+    stream = torch.cuda.current_stream()
+    for _ in range(max(warmup, 3)):
+        bt.decode(q, out)
+    torch.cuda.synchronize()
+    code, detail = bt.device_status()
+    if code:
+        raise RuntimeError(f"device status {code} ({detail})")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)]
+           for _ in range(K)]
+    # torch creates the CUDA event behind an Event on its first record: do
+    # that now, outside the timed region, so the library gets real handles.
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    if before is not None:
+        before()
+    torch.cuda.synchronize()
+    if flush is None:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(K):
+            B.kv_set_launch_events(evs[i])
+            bt.decode(q, out)
+        end.record(stream)
+        B.kv_set_launch_events(None)
+        torch.cuda.synchronize()
+        ms = start.elapsed_time(end) / K
+    else:
+        pairs = [(torch.cuda.Event(enable_timing=True),
+                  torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            flush[0].add_(1)
+            flush[1].sum()
+            pairs[i][0].record(stream)
+            B.kv_set_launch_events(evs[i])
+            bt.decode(q, out)
+            pairs[i][1].record(stream)
+        B.kv_set_launch_events(None)
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in pairs) / K
+    per_kernel = {}
+    for k, name in enumerate(["tile_tcgen05", "splitkv_mma", "lse_merge"]):
+        if k == 0 and bt.info.n_tile_items == 0:
+            continue
+        if k == 1 and bt.info.n_row_items == 0:
+            continue
+        per_kernel[name] = sum(e[2 * k].elapsed_time(e[2 * k + 1])
+                               for e in evs) / K
+    code, detail = bt.device_status()
+    if code:
+        raise RuntimeError(f"device status {code} ({detail})")
+    return ms, per_kernel, evs
+
+
+def kernel_roofline(bt, w, per_kernel, evs, peak, peak_kind):
+    """Roofline of the dominant unit.  When the tile pass runs on its side
+    stream beside the split pass, the two kernels share the GPU and each
+    one's event window includes time spent queued behind the other: the unit
+    is then the concurrent pair, its algorithmic bytes over the window from
+    the first start to the last end (per step, averaged)."""
+    alg_by = {k: item_bytes(bt.plan, bt.info, w.Hkv, w.d, bt.seq_lens,
+                            "row" if k == "splitkv_mma" else "tile")
+              for k in per_kernel if k != "lse_merge"}
+    if len(alg_by) == 2:
+        win = 0.0
+        for e in evs:
+            starts = [0.0, e[0].elapsed_time(e[2])]      # relative to tile start
+            ends = [e[0].elapsed_time(e[1]), e[0].elapsed_time(e[3])]
+            win += max(ends) - min(starts)
+        win /= len(evs)
+        alg = sum(alg_by.values())
+        kname = "tile_decode_kernel+splitkv_decode_kernel"
+        t1 = traffic_per_launch(KERNEL_NAMES["tile_tcgen05"], w.name)
+        t2 = traffic_per_launch(KERNEL_NAMES["splitkv_mma"], w.name)
+        traffic = t1 + t2 if t1 is not None and t2 is not None else None
+        dom_ms = win
+    else:
+        dom = next(iter(alg_by))
+        alg = alg_by[dom]
+        kname = KERNEL_NAMES[dom]
+        traffic = traffic_per_launch(kname, w.name)
+        dom_ms = per_kernel[dom]
+    achieved = alg / (dom_ms / 1e3) / 1e9
+    return {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
+            "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "algorithmic_bytes_per_launch": alg,
+            "ms_per_launch": round(dom_ms, 5)}
+
+
+def per_config_line(w, dev, steps, warmup, peak, peak_kind, flush, cpu):
+    """One of the other configurations, timed like the headline step (with
+    an L2 flush before every step), with the oracle's rate beside it."""
+    import torch
+    from paged_kv_cache_attn_gb300 import harness as H
+    cache = H.Cache(w, device=dev)
+    bt = cache.batch().upload()
+    q = torch.from_numpy(w.queries(bt.nb).view(np.int16)).to(dev) \
+        .view(torch.bfloat16)
+    out = torch.empty_like(q)
+    uniq = unique_kv_bytes(bt.tables, bt.seq_lens, w.Hkv, w.d)
+    ms, per_kernel, evs = time_steps(bt, q, out, steps, warmup, flush)
+    roof = kernel_roofline(bt, w, per_kernel, evs, peak, peak_kind)
+    gbs = uniq / (ms / 1e3) / 1e9
+    res = {
+        "description": w.description,
+        "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d, "branches": bt.nb,
+        "segments": int(len(bt.groups)), "unique_kv_bytes": uniq,
+        "steps": steps, "ms_per_step": round(ms, 5),
+        "value": round(gbs, 1), "unit": "GB/s",
+        "branch_queries_per_s": round(bt.nb / (ms / 1e3), 1),
+        "kernels_ms": {k: round(v, 5) for k, v in per_kernel.items()},
+        "step_roofline": {"bound": "hbm", "achieved": round(gbs, 1),
+                          "peak": peak, "unit": "GB/s",
+                          "frac": round(gbs / peak, 4)},
+        "roofline": roof,
+        "l2": "L2 flushed before every step (a 256 MB buffer written, then "
+              "another 256 MB buffer read, so no dirty line is left); each "
+              "step timed by its own events",
+        "gpu_launches": len(per_kernel) * steps,
+    }
+    if len(bt.groups):
+        res["sharing_measured_ncu"] = measured_sharing(w.name)
+    cache.close()
+    if cpu:
+        res["cpu_baseline"] = cpu_baseline(w, budget_s=5.0)
+    return res
+
 
 def run_ours(args):
     import torch
@@ -294,90 +472,21 @@ def run_ours(args):
     uniq = unique_kv_bytes(bt.tables, bt.seq_lens, w.Hkv, w.d)
     stream = torch.cuda.current_stream()
 
-    for _ in range(max(args.warmup, 3)):
-        bt.decode(q, out)
-    torch.cuda.synchronize()
-    code, detail = bt.device_status()
-    if code:
-        raise RuntimeError(f"device status {code} ({detail})")
-
-    # Timed region: K steps, per-kernel events recorded by the library.
+    # Timed region: K steps (inputs far larger than L2, no flush), the
+    # library's per-kernel events recorded on the launching streams.
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)]
-           for _ in range(K)]
-    # torch creates the CUDA event behind an Event on its first record: do
-    # that now, outside the timed region, so the library gets real handles.
-    for row in evs:
-        for e in row:
-            e.record(stream)
-    torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    if ws > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        start.record(stream)
-        for i in range(K):
-            B.kv_set_launch_events(evs[i])
-            bt.decode(q, out)
-        end.record(stream)
-        B.kv_set_launch_events(None)
-        torch.cuda.synchronize()
-    if ws > 1:
-        torch.distributed.barrier()
-    ms = start.elapsed_time(end)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    ms_step = ms / K
-    per_kernel = {}
-    names = ["tile_tcgen05", "splitkv_mma", "lse_merge"]
-    for k, name in enumerate(names):
-        if k == 0 and bt.info.n_tile_items == 0:
-            continue
-        if k == 1 and bt.info.n_row_items == 0:
-            continue
-        per_kernel[name] = sum(e[2 * k].elapsed_time(e[2 * k + 1])
-                               for e in evs) / K
-    code, detail = bt.device_status()
-    if code:
-        raise RuntimeError(f"device status {code} ({detail})")
-    launches_per_step = len(per_kernel)
-
-    # Roofline of the dominant kernel.  When the tile pass runs on its side
-    # stream beside the split pass, the two kernels share the GPU and each
-    # one's event window includes time spent queued behind the other: the
-    # unit is then the concurrent pair, its algorithmic bytes over the window
-    # from the first start to the last end (per step, averaged).
-    alg_by = {k: item_bytes(bt.plan, bt.info, w.Hkv, w.d, bt.seq_lens,
-                            "row" if k == "splitkv_mma" else "tile")
-              for k in per_kernel if k != "lse_merge"}
     peak, peak_kind = measured_peaks()
-    names = {"splitkv_mma": "splitkv_decode_kernel",
-             "tile_tcgen05": "tile_decode_kernel"}
-    if len(alg_by) == 2:
-        win = 0.0
-        for e in evs:
-            starts = [0.0, e[0].elapsed_time(e[2])]      # relative to tile start
-            ends = [e[0].elapsed_time(e[1]), e[0].elapsed_time(e[3])]
-            win += max(ends) - min(starts)
-        win /= K
-        alg = sum(alg_by.values())
-        achieved = alg / (win / 1e3) / 1e9
-        kname = "tile_decode_kernel+splitkv_decode_kernel"
-        t1 = traffic_per_launch(names["tile_tcgen05"], w.name)
-        t2 = traffic_per_launch(names["splitkv_mma"], w.name)
-        traffic = t1 + t2 if t1 is not None and t2 is not None else None
-        dom_ms = win
-    else:
-        dom = next(iter(alg_by))
-        alg = alg_by[dom]
-        achieved = alg / (per_kernel[dom] / 1e3) / 1e9
-        kname = names[dom]
-        traffic = traffic_per_launch(kname, w.name)
-        dom_ms = per_kernel[dom]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms_step, per_kernel, evs = time_steps(
+            bt, q, out, K, args.warmup,
+            before=torch.distributed.barrier if ws > 1 else None)
+    if ws > 1:
+        torch.distributed.barrier()
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    launches_per_step = len(per_kernel)
+    roof = kernel_roofline(bt, w, per_kernel, evs, peak, peak_kind)
 
     # End to end through the public API with host buffers.  Per step the
     # host builds the batch and the plan into pinned staging buffers
@@ -443,7 +552,7 @@ def run_ours(args):
 
     # Serial.
     e2e_t = []
-    for i in range(args.e2e_steps + 3):
+    for i in range(max(args.e2e_steps, 1) + 3):
         pin, dbf = bufs[0]
         torch.cuda.synchronize()
         t0 = time.perf_counter()
@@ -532,6 +641,7 @@ def run_ours(args):
             "prefix_bytes_shared": pref_shared,
             "prefix_bytes_per_branch_reread": pref_unshared,
             "prefix_bytes_factor": round(pref_unshared / max(pref_shared, 1), 2),
+            "measured_ncu": measured_sharing(w.name),
         }
 
     # NEXT-1: each branch's newest token appended and attended to in one
@@ -726,6 +836,24 @@ def run_ours(args):
         }
         c8.close()
 
+    # The other configurations, each timed on its own (N = 1 only), with the
+    # oracle's rate on the host cores beside each, and the oracle's
+    # single-thread rate on the Llama-3-8B-shaped one.
+    per_config = None
+    if args.per_config_steps > 0 and ws == 1:
+        flush = [torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+                 for _ in range(2)]
+        per_config = {}
+        for name in ("tiny_tree", "independent", "fanout", "deep_tree"):
+            per_config[name] = per_config_line(
+                W.make(name, rank), dev, args.per_config_steps, args.warmup,
+                peak, peak_kind, flush, not args.no_cpu_baseline)
+        if not args.no_cpu_baseline:
+            st = cpu_baseline(W.make("independent", rank), budget_s=6.0,
+                              threads=1)
+            per_config["independent"]["cpu_baseline_single_thread"] = st
+        del flush
+
     res = None
     if rank == 0:
         clocks = clk.summary()
@@ -755,18 +883,7 @@ def run_ours(args):
                 "parallelism": f"replicas x{ws}",
             },
             "kernels_ms": {k: round(v, 5) for k, v in per_kernel.items()},
-            "roofline": {
-                "kernel": kname,
-                "bound": "hbm",
-                "achieved": round(achieved, 1),
-                "peak": peak,
-                "peak_kind": peak_kind,
-                "unit": "GB/s",
-                "frac": round(achieved / peak, 4),
-                "traffic": traffic,
-                "algorithmic_bytes_per_launch": alg,
-                "ms_per_launch": round(dom_ms, 5),
-            },
+            "roofline": roof,
             "step_roofline": {
                 "bound": "hbm",
                 "achieved": round(uniq / (ms_step / 1e3) / 1e9, 1),
@@ -793,6 +910,7 @@ def run_ours(args):
             "offload": offload,
             "graph_replay": graph,
             "kv_e4m3": e4m3,
+            "per_config": per_config,
             "gpu_launches": launches_per_step * K,
             "clocks": clocks,
         }
@@ -886,8 +1004,37 @@ def radix_timing():
                         "(2304 then 2432 tokens), through the Python binding"}
 
 
+def profile_step(args):
+    """A few decode steps of one workload and one plan, nothing else."""
+    import torch
+    from paged_kv_cache_attn_gb300 import binding as B
+    from paged_kv_cache_attn_gb300 import harness as H
+    from paged_kv_cache_attn_gb300 import workloads as W
+    w = W.make(args.workload)
+    cache = H.Cache(w, device="cuda:0")
+    flags = B.KV_PLAN_IGNORE_GROUPS if args.profile_step == "reread" else 0
+    bt = cache.batch(flags=flags).upload()
+    q = torch.from_numpy(w.queries(bt.nb).view(np.int16)).cuda() \
+        .view(torch.bfloat16)
+    out = torch.empty_like(q)
+    for _ in range(args.steps):
+        bt.decode(q, out)
+    torch.cuda.synchronize()
+    code, detail = bt.device_status()
+    if code:
+        raise RuntimeError(f"device status {code} ({detail})")
+    print(json.dumps({"workload": w.name, "plan": args.profile_step,
+                      "tile_items": bt.info.n_tile_items,
+                      "split_items": bt.info.n_row_items,
+                      "steps": args.steps}))
+    cache.close()
+
+
 def main():
     args = parse()
+    if args.profile_step:
+        profile_step(args)
+        return
     res = run_reference(args) if args.impl == "reference" else run_ours(args)
     if res is not None:
         print(json.dumps(res, default=lambda o: o.item() if hasattr(o, "item")
