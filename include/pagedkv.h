@@ -65,6 +65,9 @@ typedef int32_t kv_status;
                                      branch re-reads its whole table) */
 #define KV_PLAN_KV_E4M3 4         /* the step reads an e4m3 pool
                                      (paged_decode_attn_e4m3) */
+#define KV_PLAN_NARROW_TILES 8    /* tcgen05 tiles of 128 rows only (no
+                                     256-row items; used to compare the two
+                                     tile kernels) */
 
 /* Element type of a pool's K and V. */
 #define KV_DTYPE_BF16 0
@@ -378,10 +381,14 @@ typedef struct kv_decode_plan_info {
   int64_t workspace_bytes; /* device workspace paged_decode_attn needs */
   int64_t partial_rows;    /* (o, m, l) partial rows in the workspace */
   int32_t n_row_items;     /* work items of the split-KV (mma.sync) kernel */
-  int32_t n_tile_items;    /* 128-row work items of the tcgen05 kernel */
+  int32_t n_tile_items;    /* work items of the tcgen05 kernels (the first
+                              n_tile_wide_items of up to 256 rows, the rest
+                              of up to 128) */
   int32_t n_merge_rows;    /* nb (one merge per branch and kv-head) */
   int32_t chunk_blocks;    /* blocks per split-KV item */
-  int32_t reserved2;       /* 0 */
+  int32_t n_tile_wide_items; /* tcgen05 items of up to 256 rows: segments of
+                                more than 128 rows (bf16), two M-tiles per
+                                item sharing every K/V load */
   int32_t flags;           /* the KV_PLAN_* flags the plan was made with */
   int32_t n_row_warp_items; /* the last n_row_warp_items of the split-KV
                                items are short (at most 16 blocks): the bf16

@@ -31,6 +31,7 @@ KV_STOP_EVICTED_LEAVES = 1
 KV_PLAN_NO_TENSOR_CORES = 1
 KV_PLAN_IGNORE_GROUPS = 2
 KV_PLAN_KV_E4M3 = 4
+KV_PLAN_NARROW_TILES = 8
 KV_DTYPE_BF16 = 0
 KV_DTYPE_E4M3 = 1
 
@@ -63,7 +64,7 @@ class kv_decode_plan_info(C.Structure):
     _fields_ = [("plan_ints", C.c_int64), ("workspace_bytes", C.c_int64),
                 ("partial_rows", C.c_int64), ("n_row_items", C.c_int32),
                 ("n_tile_items", C.c_int32), ("n_merge_rows", C.c_int32),
-                ("chunk_blocks", C.c_int32), ("reserved2", C.c_int32),
+                ("chunk_blocks", C.c_int32), ("n_tile_wide_items", C.c_int32),
                 ("flags", C.c_int32), ("n_row_warp_items", C.c_int32),
                 ("reserved", C.c_int32)]
 

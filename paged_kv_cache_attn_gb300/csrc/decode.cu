@@ -571,12 +571,20 @@ cudaError_t launch_tile_items(const CUtensorMap& tk, const CUtensorMap& tv,
                               const SplitParams& sp, const WorkItem* items,
                               int n_items, int d, cudaStream_t stream);
 
+// Tensor-core kernel for items of up to 256 rows (two M-tiles sharing each
+// K/V load); defined in decode_tc_wide.cu.
+cudaError_t launch_tile_wide_items(const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const SplitParams& sp, const WorkItem* items,
+                                   int n_items, int d, cudaStream_t stream);
+
 // Second stream (and fork / join events) per device: the tensor-core tile
 // pass runs beside the split-KV pass so that the tile kernel's tensor work
 // overlaps the split kernel's HBM streaming on the same SMs.
+// A step with both 256-row and 128-row tile items runs the two tile kernels
+// on two such streams, side by side.
 struct SideStream {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaStream_t stream = nullptr, stream2 = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, join2 = nullptr;
 };
 
 kv_status side_stream(SideStream** out) {
@@ -595,9 +603,13 @@ kv_status side_stream(SideStream** out) {
     cudaDeviceGetStreamPriorityRange(&lo, &hi);
     e = cudaStreamCreateWithPriority(&s.stream, cudaStreamNonBlocking, hi);
     if (e == cudaSuccess)
+      e = cudaStreamCreateWithPriority(&s.stream2, cudaStreamNonBlocking, hi);
+    if (e == cudaSuccess)
       e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
     if (e == cudaSuccess)
       e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+    if (e == cudaSuccess)
+      e = cudaEventCreateWithFlags(&s.join2, cudaEventDisableTiming);
     if (e != cudaSuccess) {
       s.stream = nullptr;
       return fail(KV_ERR_CUDA, "side stream: %s", cudaGetErrorString(e));
@@ -666,6 +678,11 @@ static kv_status decode_impl(
                                          : "plan was made for an e4m3 pool");
   if (info->n_tile_items != 0 && d != 128)
     return fail(KV_ERR_INVALID_ARG, "tensor-core tiles need head_dim 128");
+  if (info->n_tile_wide_items < 0 ||
+      info->n_tile_wide_items > info->n_tile_items ||
+      (e4m3 && info->n_tile_wide_items != 0))
+    return fail(KV_ERR_INVALID_ARG, "plan info: bad n_tile_wide_items %d",
+                info->n_tile_wide_items);
   if ((uintptr_t)workspace & 255)
     return fail(KV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   if (!std::isfinite(scale) || !(scale > 0.f))
@@ -733,13 +750,20 @@ static kv_status decode_impl(
       return fail(KV_ERR_CUDA, "e4m3 append launch failed (cuda %d)", err);
   }
   // With both passes present the tile pass forks onto the side stream and
-  // joins back before the merge.
+  // joins back before the merge; 256-row and 128-row tile items, when a step
+  // has both, run on two side streams.
   pkv::SideStream* side = nullptr;
-  const bool fork = info->n_tile_items > 0 && info->n_row_items > 0;
+  const int n_wide = e4m3 ? 0 : info->n_tile_wide_items;
+  const int n_narrow = info->n_tile_items - n_wide;
+  const bool two_tile = n_wide > 0 && n_narrow > 0;
+  const bool fork =
+      info->n_tile_items > 0 && (info->n_row_items > 0 || two_tile);
   if (fork) {
     if (kv_status s2 = pkv::side_stream(&side)) return s2;
     e = cudaEventRecord(side->fork, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+    if (e == cudaSuccess && two_tile)
+      e = cudaStreamWaitEvent(side->stream2, side->fork, 0);
     if (e != cudaSuccess)
       return fail(KV_ERR_CUDA, "fork: %s", cudaGetErrorString(e));
   }
@@ -747,10 +771,23 @@ static kv_status decode_impl(
     cudaStream_t ts = fork ? side->stream : st;
     pkv::mark(0, ts);
     const auto* titems = reinterpret_cast<const pkv::WorkItem*>(plan + off_tile);
-    e = e4m3 ? pkv::launch_tile_e4m3(sp, titems, info->n_tile_items, k_pool,
-                                     v_pool, kv_scales, ts)
-             : pkv::launch_tile_items(tk_tiles, tv_tiles, sp, titems,
-                                      info->n_tile_items, d, ts);
+    if (e4m3) {
+      e = pkv::launch_tile_e4m3(sp, titems, info->n_tile_items, k_pool, v_pool,
+                                kv_scales, ts);
+    } else {
+      e = cudaSuccess;
+      if (n_wide > 0)
+        e = pkv::launch_tile_wide_items(tk_tiles, tv_tiles, sp, titems, n_wide,
+                                        d, ts);
+      if (e == cudaSuccess && n_narrow > 0)
+        e = pkv::launch_tile_items(tk_tiles, tv_tiles, sp, titems + n_wide,
+                                   n_narrow, d, two_tile ? side->stream2 : ts);
+      // The tile pass ends when both of its streams have.
+      if (e == cudaSuccess && two_tile) {
+        e = cudaEventRecord(side->join2, side->stream2);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(ts, side->join2, 0);
+      }
+    }
     pkv::mark(1, ts);
     if (e != cudaSuccess)
       return fail(KV_ERR_CUDA, "tile kernel: %s", cudaGetErrorString(e));

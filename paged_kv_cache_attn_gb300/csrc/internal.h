@@ -91,6 +91,7 @@ struct MergeEntry {
 
 constexpr bool kTensorCoreKernel = true;  // tcgen05 tile kernel available
 constexpr int kTileRows = 128;      // rows of a tcgen05 tile
+constexpr int kWideRows = 256;      // rows of a two-M-tile tcgen05 item
 constexpr int kRowTile = 16;        // rows of an mma.sync tile
 constexpr int kMinTensorRows = 65;  // segments with more rows go to tcgen05
 constexpr int kWarpItemBlocks = 16; // split-KV items this short run per warp

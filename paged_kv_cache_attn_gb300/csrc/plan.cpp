@@ -21,21 +21,26 @@ namespace {
 
 struct Unit {
   int32_t branch0, rows, blk_begin, blk_end, masked;
-  bool tile;  // tcgen05 128-row tiles
+  bool tile;  // tcgen05 tiles
+  bool wide;  // ... of 256 rows (two M-tiles per item)
 };
+
+int rows_per(const Unit& u) {
+  return u.wide ? pkv::kWideRows : u.tile ? pkv::kTileRows : pkv::kRowTile;
+}
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int32_t pick_chunk(const std::vector<Unit>& units, bool tile, int Hkv,
                    int num_sms, int32_t start) {
-  const int rows_per = tile ? pkv::kTileRows : pkv::kRowTile;
   int32_t chunk = start;
   for (;;) {
     int64_t items = 0;
     for (const Unit& u : units) {
       if (u.tile != tile) continue;
+      // A 256-row item counts as two 128-row tiles: it carries their work.
       items += ceil_div(u.blk_end - u.blk_begin, chunk) *
-               ceil_div(u.rows, rows_per) * Hkv;
+               ceil_div(u.rows, rows_per(u)) * Hkv * (u.wide ? 2 : 1);
     }
     if (chunk <= 8 || items >= 2LL * num_sms) return chunk;
     chunk /= 2;
@@ -78,11 +83,17 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   std::vector<Unit> units;
   const bool use_groups = !(flags & KV_PLAN_IGNORE_GROUPS);
   if (flags & ~(KV_PLAN_NO_TENSOR_CORES | KV_PLAN_IGNORE_GROUPS |
-                KV_PLAN_KV_E4M3))
+                KV_PLAN_KV_E4M3 | KV_PLAN_NARROW_TILES))
     return fail(KV_ERR_INVALID_ARG, "unknown plan flags 0x%x", flags);
   // The tcgen05 tile kernels are built for head_dim 128 (bf16 and e4m3).
   const bool allow_tc = pkv::kTensorCoreKernel && d == 128 &&
                         !(flags & KV_PLAN_NO_TENSOR_CORES);
+  // Segments of 129 to 256 rows run as one two-M-tile item per block range
+  // (bf16 only), which reads the range once for all of their rows.  Larger
+  // segments keep 128-row tiles: with no room in TMEM to double-buffer S
+  // for two M-tiles, a two-M-tile item costs more SM time per row.
+  const bool allow_wide =
+      allow_tc && !(flags & (KV_PLAN_KV_E4M3 | KV_PLAN_NARROW_TILES));
   units.reserve((size_t)(use_groups ? n_groups : 0) + nb);
   if (use_groups && n_groups > 0) {
     // Each row's segment ranges, grouped by row with a counting sort (one
@@ -102,8 +113,10 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
                       "segment %d covers a block not full for row %d", i, b);
         ++first[b + 1];
       }
-      units.push_back({bb, bc * G, kb, kb + kc, 0,
-                       allow_tc && bc * G >= pkv::kMinTensorRows});
+      const bool tc = allow_tc && bc * G >= pkv::kMinTensorRows;
+      units.push_back({bb, bc * G, kb, kb + kc, 0, tc,
+                       tc && allow_wide && bc * G > pkv::kTileRows &&
+                           bc * G <= pkv::kWideRows});
     }
     for (int32_t b = 0; b < nb; ++b) first[b + 1] += first[b];
     std::vector<std::pair<int32_t, int32_t>> ranges(first[nb]);
@@ -129,7 +142,7 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   }
   for (int32_t b = 0; b < nb; ++b) {
     if (shared_end[b] < nblk[b])
-      units.push_back({b, G, shared_end[b], nblk[b], 1, false});
+      units.push_back({b, G, shared_end[b], nblk[b], 1, false, false});
   }
 
   // Split-KV items: up to 128 blocks.  Tile items: up to 256 blocks (their
@@ -144,28 +157,28 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   std::stable_sort(units.begin(), units.end(), [](const Unit& x, const Unit& y) {
     return (x.blk_end - x.blk_begin) > (y.blk_end - y.blk_begin);
   });
-  std::vector<pkv::WorkItem> row_items, tile_items;
+  std::vector<pkv::WorkItem> row_items, tile_items, wide_items;
   struct Tagged { int32_t branch; pkv::MergeEntry e; };
   std::vector<Tagged> merge_flat;
   {
     // Exact item counts and a bound on the merge entries, so that the loop
     // below never reallocates.
-    int64_t n_row = 0, n_tile = 0, n_merge = 0;
+    int64_t n_row = 0, n_tile = 0, n_wide = 0, n_merge = 0;
     for (const Unit& u : units) {
-      const int rows_per = u.tile ? pkv::kTileRows : pkv::kRowTile;
       const int64_t nch =
           ceil_div(u.blk_end - u.blk_begin, u.tile ? chunk_tile : chunk_rows);
-      const int64_t tiles = ceil_div(u.rows, rows_per);
-      (u.tile ? n_tile : n_row) += nch * tiles * Hkv;
-      n_merge += nch * tiles * (rows_per / G + 2);
+      const int64_t tiles = ceil_div(u.rows, rows_per(u));
+      (u.wide ? n_wide : u.tile ? n_tile : n_row) += nch * tiles * Hkv;
+      n_merge += nch * tiles * (rows_per(u) / G + 2);
     }
     row_items.reserve(n_row);
-    tile_items.reserve(n_tile);
+    tile_items.reserve(n_wide + n_tile);
+    wide_items.reserve(n_wide);
     merge_flat.reserve(n_merge);
   }
   int64_t prow = 0;
   for (const Unit& u : units) {
-    const int rows_per = u.tile ? pkv::kTileRows : pkv::kRowTile;
+    const int rp = rows_per(u);
     const int32_t chunk = u.tile ? chunk_tile : chunk_rows;
     const int32_t len = u.blk_end - u.blk_begin;
     const int32_t nch = (int32_t)ceil_div(len, chunk);
@@ -173,13 +186,13 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
       // Even split of the range into nch pieces.
       const int32_t lo = u.blk_begin + (int32_t)((int64_t)len * c / nch);
       const int32_t hi = u.blk_begin + (int32_t)((int64_t)len * (c + 1) / nch);
-      for (int32_t row0 = 0; row0 < u.rows; row0 += rows_per) {
-        const int32_t nrows = std::min(rows_per, u.rows - row0);
+      for (int32_t row0 = 0; row0 < u.rows; row0 += rp) {
+        const int32_t nrows = std::min(rp, u.rows - row0);
         const int64_t base0 = prow;
         for (int32_t g = 0; g < Hkv; ++g) {
           pkv::WorkItem it{u.branch0, g, row0, nrows, lo, hi,
                            (int32_t)(base0 + (int64_t)g * nrows), u.masked};
-          (u.tile ? tile_items : row_items).push_back(it);
+          (u.wide ? wide_items : u.tile ? tile_items : row_items).push_back(it);
         }
         prow += (int64_t)nrows * Hkv;
         if (prow > INT32_MAX)
@@ -204,6 +217,9 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
         return it.blk_end - it.blk_begin > pkv::kWarpItemBlocks;
       });
   const int32_t n_warp_items = (int32_t)(row_items.end() - first_short);
+  // The 256-row tile items go first in the tile list.
+  const int32_t n_wide_items = (int32_t)wide_items.size();
+  tile_items.insert(tile_items.begin(), wide_items.begin(), wide_items.end());
   const int64_t n_csr = (int64_t)merge_flat.size();
   const int64_t off_row = pkv::kPlanHeaderInts;
   const int64_t off_tile = off_row + 8 * (int64_t)row_items.size();
@@ -221,7 +237,7 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   info->n_tile_items = (int32_t)tile_items.size();
   info->n_merge_rows = nb;
   info->chunk_blocks = chunk_rows;
-  info->reserved2 = 0;
+  info->n_tile_wide_items = n_wide_items;
   info->flags = flags;
   if (!plan) return KV_OK;
   if (plan_cap < total)

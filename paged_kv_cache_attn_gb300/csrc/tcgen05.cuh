@@ -39,6 +39,18 @@ __device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a,
       : "memory");
 }
 
+// D (+)= A B, kind::f16, with A and B both from shared-memory descriptors.
+__device__ __forceinline__ void umma_ss(uint32_t tmem_d, uint64_t a, uint64_t b,
+                                        uint32_t id, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          tmem_d),
+      "l"(a), "l"(b), "r"(id), "r"(accumulate)
+      : "memory");
+}
+
 // Instruction descriptor for kind::f16 with A and B both K-major and f16
 // (format code 0), fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_k0(int M, int N) {

@@ -58,6 +58,8 @@ SMALL = {
     "fanout_3tiles": lambda: W.fanout(n_roots=1, root_tokens=512, fan=40,
                                       min_suffix=1, max_suffix=50, Hq=64,
                                       Hkv=8),
+    "fanout_256": lambda: W.fanout(n_roots=2, root_tokens=777, fan=64,
+                                   min_suffix=1, max_suffix=90),
     "gqa_2": lambda: W.independent(n_seqs=3, min_len=17, max_len=300, Hq=8,
                                    Hkv=4, d=64),
     "gqa_16": lambda: W.fanout(n_roots=1, root_tokens=64, fan=3,
@@ -73,7 +75,8 @@ def built():
 
 @pytest.mark.parametrize("name", list(SMALL))
 @pytest.mark.parametrize("flags", [0, B.KV_PLAN_IGNORE_GROUPS,
-                                   B.KV_PLAN_NO_TENSOR_CORES])
+                                   B.KV_PLAN_NO_TENSOR_CORES,
+                                   B.KV_PLAN_NARROW_TILES])
 def test_decode_matches_oracle(built, name, flags):
     w = SMALL[name]()
     cache = H.Cache(w)

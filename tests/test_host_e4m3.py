@@ -73,13 +73,26 @@ def segment_plan(flags):
     return B.paged_decode_plan(nb, 64, 8, 128, mb, lens, groups, 152, flags)
 
 
-def test_plan_records_its_flags():
+def test_plan_records_its_flags_and_keeps_e4m3_tiles_narrow():
     _, bf = segment_plan(0)
     _, e8 = segment_plan(B.KV_PLAN_KV_E4M3)
     assert bf.flags == 0 and e8.flags == B.KV_PLAN_KV_E4M3
-    # the same rows and blocks are covered either way: 3 tiles x 8 heads
-    assert e8.n_tile_items > 0 and e8.n_tile_items == bf.n_tile_items
+    # 320 rows: three 128-row tiles per block range and kv-head either way
+    assert bf.n_tile_wide_items == 0 == e8.n_tile_wide_items
+    assert e8.n_tile_items == bf.n_tile_items > 0
     assert e8.n_tile_items == 3 * 8 * (e8.n_tile_items // 24)
+    # 256 rows: one two-M-tile item in bf16 (not in e4m3, nor in a narrow
+    # plan)
+    nb, mb = 32, 36
+    lens = np.full(nb, 36 * 16, dtype=np.int32)
+    groups = np.array([[0, nb, 0, 32]], dtype=np.int32)
+    plans = {f: B.paged_decode_plan(nb, 64, 8, 128, mb, lens, groups, 152, f)[1]
+             for f in (0, B.KV_PLAN_NARROW_TILES, B.KV_PLAN_KV_E4M3)}
+    w = plans[0]
+    assert w.n_tile_items == w.n_tile_wide_items > 0
+    for f in (B.KV_PLAN_NARROW_TILES, B.KV_PLAN_KV_E4M3):
+        assert plans[f].n_tile_wide_items == 0
+        assert plans[f].n_tile_items == 2 * w.n_tile_items
     _, nt = segment_plan(B.KV_PLAN_KV_E4M3 | B.KV_PLAN_NO_TENSOR_CORES)
     assert nt.n_tile_items == 0
     assert code(lambda: segment_plan(64)) == B.KV_ERR_INVALID_ARG

@@ -319,21 +319,28 @@ def test_short_split_items_keep_their_order():
     assert sorted(base.tolist()) == sorted(set(base.tolist()))
 
 
-def test_multi_tile_segments_split_into_128_row_tiles():
-    # 40 branches x 8 q-heads = 320 rows: 128-row tiles of 128, 128 and 64
-    # rows, each over every block range and kv-head of the segment.
-    w = W.fanout(n_roots=1, root_tokens=512, fan=40, min_suffix=1,
+@pytest.mark.parametrize("fan,flags,want", [
+    (40, 0, [(0, 128), (128, 128), (256, 64)]),        # 320 rows
+    (30, 0, [(0, 240)]),                                # one two-M-tile item
+    (30, B.KV_PLAN_NARROW_TILES, [(0, 128), (128, 112)]),
+])
+def test_multi_tile_segments_split_into_row_tiles(fan, flags, want):
+    # fan branches x 8 q-heads, over every block range and kv-head of the
+    # segment: a segment of 129-256 rows is one two-M-tile item (listed first,
+    # counted in n_tile_wide_items) unless the plan asks for narrow tiles; a
+    # larger one is cut into 128-row tiles.
+    w = W.fanout(n_roots=1, root_tokens=512, fan=fan, min_suffix=1,
                  max_suffix=50, Hq=64, Hkv=8)
-    bt = H.Cache(w, with_data=False).batch(num_sms=152)
-    assert bt.info.reserved2 == 0
+    bt = H.Cache(w, with_data=False).batch(num_sms=152, flags=flags)
     rows, tiles, ptr, ent = decode_plan(bt.plan, bt.info, bt.nb, w.Hq, w.Hkv)
+    assert bt.info.n_tile_wide_items == (len(tiles) if len(want) == 1 else 0)
     ranges = {(int(t[4]), int(t[5])) for t in tiles}
-    assert len(tiles) == 3 * 8 * len(ranges)
+    assert len(tiles) == len(want) * 8 * len(ranges)
     for lo, hi in ranges:
         for g in range(8):
             got = sorted((int(t[2]), int(t[3])) for t in tiles
                          if (t[4], t[5]) == (lo, hi) and t[1] == g)
-            assert got == [(0, 128), (128, 128), (256, 64)]
+            assert got == want
 
 
 def test_plan_rejects_bad_input():
