@@ -95,6 +95,7 @@ constexpr int kWideRows = 256;      // rows of a two-M-tile tcgen05 item
 constexpr int kRowTile = 16;        // rows of an mma.sync tile
 constexpr int kMinTensorRows = 65;  // segments with more rows go to tcgen05
 constexpr int kWarpItemBlocks = 16; // split-KV items this short run per warp
+constexpr int kSplitCtasPerSm = 3;  // resident bf16 split-KV CTAs per SM
 
 // Workspace layout (bytes): status word block, then (m, l) pairs, then o rows.
 constexpr size_t kStatusBytes = 256;

@@ -209,14 +209,19 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
       }
     }
   }
-  // Short split-KV items go last (stable): the bf16 split-KV kernel runs
-  // them one per warp, four to a CTA.  An item's partial rows do not depend
-  // on its position, so the merge lists stand.
+  // Short split-KV items go last (stable).  When there are more of them
+  // than two waves of split-KV CTAs would hold, the bf16 split-KV kernel runs
+  // them one per warp, four to a CTA (a warp takes a short item about as
+  // long as a CTA takes a long one, but four times as many run at once);
+  // fewer of them run one per CTA, which ends the step's last wave sooner.
+  // An item's partial rows do not depend on its position, so the merge
+  // lists stand.
   const auto first_short = std::stable_partition(
       row_items.begin(), row_items.end(), [](const pkv::WorkItem& it) {
         return it.blk_end - it.blk_begin > pkv::kWarpItemBlocks;
       });
-  const int32_t n_warp_items = (int32_t)(row_items.end() - first_short);
+  int32_t n_warp_items = (int32_t)(row_items.end() - first_short);
+  if (n_warp_items <= 2 * pkv::kSplitCtasPerSm * num_sms) n_warp_items = 0;
   // The 256-row tile items go first in the tile list.
   const int32_t n_wide_items = (int32_t)wide_items.size();
   tile_items.insert(tile_items.begin(), wide_items.begin(), wide_items.end());
