@@ -145,11 +145,19 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
       units.push_back({b, G, shared_end[b], nblk[b], 1, false, false});
   }
 
-  // Split-KV items: up to 128 blocks.  Tile items: up to 256 blocks (their
-  // 128-row partials are large, so fewer, longer items pay).  Each is halved
-  // while there are fewer than two items per SM.
+  // Split-KV items: up to 128 blocks, halved while there are fewer than two
+  // items per SM.  Tile items: up to 256 blocks.  A tile item carries several
+  // microseconds of fixed cost (TMEM, barriers, Q, the first loads, the
+  // epilogue) and holds a whole SM, so fewer, longer tile items pay: the
+  // split-KV pass streams on the SMs they leave free (measured on the
+  // fan-out tree: 256 tile items of 32 blocks 0.238 ms, 64 of 128 blocks
+  // 0.215 ms).  Only a step with no split-KV items at all halves them to
+  // fill the GPU.
+  bool any_rows = false;
+  for (const Unit& u : units) any_rows |= !u.tile;
   const int32_t chunk_rows = pick_chunk(units, false, Hkv, num_sms, 128);
-  const int32_t chunk_tile = pick_chunk(units, true, Hkv, num_sms, 256);
+  const int32_t chunk_tile =
+      any_rows ? 256 : pick_chunk(units, true, Hkv, num_sms, 256);
 
   // Longest units first: their items come first, so the last wave of each
   // kernel is made of the short ones.  (Items of one unit have equal length
