@@ -232,8 +232,8 @@ def measured_sharing(workload):
         return None
     return {"case": workload if workload in d else workload + "_quarter",
             "branch_sharing_factor": e["branch_sharing_factor"],
+            "prefix_bytes_to_sms_factor": e["prefix_tma_factor"],
             "prefix_l2_requests_factor": e["prefix_l2_tex_factor"],
-            "prefix_l2_sectors_factor": e["prefix_l2_factor"],
             "prefix_dram_factor": e["prefix_dram_factor"],
             "source": "profiles/ncu_sharing.json"}
 
@@ -304,6 +304,14 @@ def cpu_baseline(w, budget_s=12.0, threads=None):
 
 KERNEL_NAMES = {"splitkv_mma": "splitkv_decode_kernel",
                 "tile_tcgen05": "tile_decode_kernel"}
+
+
+def tile_kernel_name(info):
+    """The tcgen05 kernel(s) a plan's tile items run on."""
+    n_wide = info.n_tile_wide_items
+    names = (["tile_wide_kernel"] if n_wide else []) + \
+        (["tile_decode_kernel"] if info.n_tile_items > n_wide else [])
+    return "+".join(names)
 
 
 def time_steps(bt, q, out, K, warmup, flush=None, before=None):
@@ -409,10 +417,12 @@ def kernel_roofline(bt, w, per_kernel, evs, peak, peak_kind):
             win += max(ends) - min(starts)
         win /= len(evs)
         alg = sum(alg_by.values())
-        kname = "tile_decode_kernel+splitkv_decode_kernel"
-        t1 = traffic_per_launch(KERNEL_NAMES["tile_tcgen05"], w.name)
+        tname = tile_kernel_name(bt.info)
+        kname = tname + "+splitkv_decode_kernel"
+        ts = [traffic_per_launch(k, w.name) for k in tname.split("+")]
         t2 = traffic_per_launch(KERNEL_NAMES["splitkv_mma"], w.name)
-        traffic = t1 + t2 if t1 is not None and t2 is not None else None
+        traffic = (sum(ts) + t2 if None not in ts and t2 is not None
+                   else None)
         dom_ms = win
     else:
         dom = next(iter(alg_by))
