@@ -559,7 +559,7 @@ cudaError_t launch_merge(const MergeParams& mp, cudaStream_t stream) {
 // Split-KV kernel over an e4m3 pool; defined in decode_e4m3.cu.
 cudaError_t launch_split_e4m3(const SplitParams& sp, const void* k8,
                               const void* v8, const void* scales, int n_items,
-                              int d, cudaStream_t stream);
+                              int n_warp_items, int d, cudaStream_t stream);
 
 // Tensor-core tile kernel over an e4m3 pool; defined in decode_tc_e4m3.cu.
 cudaError_t launch_tile_e4m3(const SplitParams& sp, const WorkItem* items,
@@ -802,7 +802,8 @@ static kv_status decode_impl(
     pkv::mark(2, st);
     if (e4m3)
       e = pkv::launch_split_e4m3(sp, k_pool, v_pool, kv_scales,
-                                 info->n_row_items, d, st);
+                                 info->n_row_items, info->n_row_warp_items, d,
+                                 st);
     else
       e = d == 128 ? pkv::launch_split<128>(tk, tv, sp, info->n_row_items,
                                             info->n_row_warp_items, st)

@@ -71,11 +71,15 @@ struct E4m3Cfg {
 
 constexpr int kE4m3Stages = 4;
 
-template <int D, int NS>
+// kPerWarp: every warp takes a (short) item of its own, item
+// item_base + 4 * blockIdx.x + warp, and writes its partial rows itself; a
+// separate instantiation so that the CTA-wide one keeps its registers.
+template <int D, int NS, bool kPerWarp>
 __global__ void __launch_bounds__(128, 3)
     splitkv_e4m3_kernel(const SplitParams p, const uint8_t* __restrict__ k8,
                         const uint8_t* __restrict__ v8,
-                        const float4* __restrict__ scales) {
+                        const float4* __restrict__ scales, int item_base,
+                        int n_items) {
   using C = E4m3Cfg<D, NS>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[C::kWarps][NS];
@@ -87,25 +91,32 @@ __global__ void __launch_bounds__(128, 3)
   const uint32_t base = (smem_u32(smem_raw) + 127u) & ~127u;
   float* base_ptr =
       reinterpret_cast<float*>(smem_raw + (base - smem_u32(smem_raw)));
-  const WorkItem it = p.items[blockIdx.x];
-  if (!item_ok(it, p, 16)) {
-    if (threadIdx.x == 0)
-      record_status(p.status, KV_ERR_DEVICE, -1 - (int)blockIdx.x);
-    return;
+  const int idx = kPerWarp ? item_base + 4 * (int)blockIdx.x + warp
+                           : item_base + (int)blockIdx.x;
+  const WorkItem it = p.items[idx < n_items ? idx : 0];
+  bool have = idx < n_items;
+  if (have && !item_ok(it, p, 16)) {
+    if (kPerWarp ? lane == 0 : threadIdx.x == 0)
+      record_status(p.status, KV_ERR_DEVICE, -1 - idx);
+    have = false;
   }
+  if (!kPerWarp && !have) return;  // the whole CTA, before any barrier
   if (threadIdx.x == 0) {
     for (int w = 0; w < C::kWarps; ++w)
       for (int s = 0; s < NS; ++s) mbar_init(smem_u32(&bars[w][s]), 1);
     fence_mbar_init();
   }
   __syncthreads();
+  if (!have) return;  // a warp without an item (no CTA barrier follows)
 
   const int G = p.G;
   const int seq_len = it.masked ? p.seq_lens[it.branch0] : 0x7fffffff;
   const int32_t* table = p.tables + (int64_t)it.branch0 * p.max_blocks;
   const int nblk = it.blk_end - it.blk_begin;
-  const int my_n =
-      nblk > warp ? (nblk - warp + C::kWarps - 1) / C::kWarps : 0;
+  // This warp's blocks of the item: first, first + stride, ...
+  const int first = kPerWarp ? 0 : warp;
+  constexpr int stride = kPerWarp ? 1 : C::kWarps;
+  const int my_n = nblk > first ? (nblk - first + stride - 1) / stride : 0;
   const uint32_t ring = base + warp * NS * C::kStage;
   const uint32_t bar0 = smem_u32(&bars[warp][0]);
 
@@ -115,7 +126,7 @@ __global__ void __launch_bounds__(128, 3)
     if ((k >> 5) != twin) {
       twin = k >> 5;
       const int kk = (twin << 5) + lane;
-      tcache = kk < my_n ? table[it.blk_begin + warp + C::kWarps * kk] : 0;
+      tcache = kk < my_n ? table[it.blk_begin + first + stride * kk] : 0;
     }
     const int phys = __shfl_sync(0xffffffffu, tcache, k & 31);
     const bool ok = phys >= 0 && (int64_t)phys < p.num_blocks;
@@ -226,7 +237,7 @@ __global__ void __launch_bounds__(128, 3)
       if (u < nblk2) {
         if (!mbar_wait(bar0 + stg[u] * 8, ((k + u) / NS) & 1)) timed_out = true;
         use[u] = !((bad >> stg[u]) & 1);
-        const int j = it.blk_begin + warp + C::kWarps * (k + u);
+        const int j = it.blk_begin + first + stride * (k + u);
         const int n = seq_len - j * 16;
         nv[u] = use[u] ? (n > 16 ? 16 : n) : 0;
         if (use[u]) scl[u] = lds64f(ring + stg[u] * C::kStage + 2 * C::kTile);
@@ -391,6 +402,29 @@ __global__ void __launch_bounds__(128, 3)
     l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], 2);
   }
 
+  if (kPerWarp) {
+    // The warp's own item: its state is the partial result (O back to plain
+    // units, x vref).  Lane (gq, tq) holds rows gq and gq + 8, columns
+    // 8 nt + 2 tq and + 1.
+    float* dst = p.o + (int64_t)it.prow_base * D;
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) {
+      const int col = nt * 8 + 2 * tq;
+      if (gq < it.nrows)
+        *reinterpret_cast<float2*>(dst + gq * D + col) =
+            make_float2(o[nt][0] * vref, o[nt][1] * vref);
+      if (gq + 8 < it.nrows)
+        *reinterpret_cast<float2*>(dst + (gq + 8) * D + col) =
+            make_float2(o[nt][2] * vref, o[nt][3] * vref);
+    }
+    if (tq == 0) {
+      if (gq < it.nrows) p.ml[it.prow_base + gq] = make_float2(m_r[0], l_r[0]);
+      if (gq + 8 < it.nrows)
+        p.ml[it.prow_base + gq + 8] = make_float2(m_r[1], l_r[1]);
+    }
+    return;
+  }
+
   // Combine the four warps' partial states through shared memory; O goes
   // back to plain units (x vref).
   __syncthreads();
@@ -446,21 +480,37 @@ __global__ void __launch_bounds__(128, 3)
   }
 }
 
+// The long items one per CTA, then the last n_warp_items (short) one per
+// warp, four to a CTA, on the same stream.
 template <int D>
 cudaError_t launch_t(const SplitParams& sp, const void* k8, const void* v8,
-                     const void* scales, int n_items, cudaStream_t stream) {
+                     const void* scales, int n_items, int n_warp_items,
+                     cudaStream_t stream) {
   using C = E4m3Cfg<D, kE4m3Stages>;
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        splitkv_e4m3_kernel<D, kE4m3Stages>,
+    cudaError_t e = cudaFuncSetAttribute(
+        splitkv_e4m3_kernel<D, kE4m3Stages, false>,
         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(splitkv_e4m3_kernel<D, kE4m3Stages, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  splitkv_e4m3_kernel<D, kE4m3Stages><<<n_items, 128, C::kSmem, stream>>>(
-      sp, static_cast<const uint8_t*>(k8), static_cast<const uint8_t*>(v8),
-      static_cast<const float4*>(scales));
+  if (n_warp_items < 0 || n_warp_items > n_items) return cudaErrorInvalidValue;
+  const int n_long = n_items - n_warp_items;
+  const auto* k = static_cast<const uint8_t*>(k8);
+  const auto* v = static_cast<const uint8_t*>(v8);
+  const auto* s = static_cast<const float4*>(scales);
+  if (n_long > 0)
+    splitkv_e4m3_kernel<D, kE4m3Stages, false>
+        <<<n_long, 128, C::kSmem, stream>>>(sp, k, v, s, 0, n_items);
+  if (n_warp_items > 0)
+    splitkv_e4m3_kernel<D, kE4m3Stages, true>
+        <<<(n_warp_items + 3) / 4, 128, C::kSmem, stream>>>(sp, k, v, s,
+                                                            n_long, n_items);
   return cudaGetLastError();
 }
 
@@ -468,9 +518,11 @@ cudaError_t launch_t(const SplitParams& sp, const void* k8, const void* v8,
 
 cudaError_t launch_split_e4m3(const SplitParams& sp, const void* k8,
                               const void* v8, const void* scales, int n_items,
-                              int d, cudaStream_t stream) {
-  return d == 128 ? launch_t<128>(sp, k8, v8, scales, n_items, stream)
-                  : launch_t<64>(sp, k8, v8, scales, n_items, stream);
+                              int n_warp_items, int d, cudaStream_t stream) {
+  return d == 128 ? launch_t<128>(sp, k8, v8, scales, n_items, n_warp_items,
+                                  stream)
+                  : launch_t<64>(sp, k8, v8, scales, n_items, n_warp_items,
+                                 stream);
 }
 
 }  // namespace pkv
