@@ -428,12 +428,13 @@ kv_status paged_decode_attn_workspace_size(const kv_decode_plan_info* info,
  * these seq_lens/groups, with *info its host info.  Output: out
  * [nb][Hq][head_dim] bf16.  workspace: device, >= info->workspace_bytes,
  * 256-byte aligned, no initial contents needed.  Shared-prefix blocks are read
- * once per segment (tensor cores for segments of >= 65 rows).  When a step has
- * both tensor-core tiles and split-KV items, the tile pass runs on a
- * library-owned second stream (highest priority) forked from and joined back
- * into `stream`
- * (event record / wait), so that the two passes overlap; all work is still
- * ordered after earlier work on `stream` and before later work on it.
+ * once per tile item (tensor cores for segments of >= 65 rows: one item per
+ * 256 rows for segments of 129-256 rows, one per 128 rows otherwise).  When a
+ * step has both tensor-core tiles and split-KV items (or both sizes of
+ * tile items), the tile pass runs on one or two library-owned streams
+ * (highest priority) forked from and joined back into `stream` (event
+ * record / wait), so that the passes overlap; all work is still ordered
+ * after earlier work on `stream` and before later work on it.
  * Error behaviour: argument errors return INVALID_ARG before any launch; a
  * block id outside [0, num_blocks) or a timed-out wait is recorded in the
  * workspace status word (the access is skipped, the output is then

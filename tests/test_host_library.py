@@ -416,3 +416,25 @@ def test_batched_append_is_all_or_nothing():
             B.kv_get_free_stack(h).tolist()) == before
     assert B.kv_get_block_table(h, a)[1] == 20
     B.kv_pool_destroy(h)
+
+
+def test_tile_items_stay_long_when_the_step_has_split_items():
+    """Tile items span 256 blocks (or the whole segment) whenever the step
+    also has split-KV items, however few SMs would be busy; a step made of
+    segments only halves them until there are two items per SM."""
+    nb, mb = 16, 600
+    lens = np.full(nb, 600 * 16, dtype=np.int32)
+    # 16 branches x 8 q-heads = 128 rows sharing 512 full blocks
+    shared = np.array([[0, nb, 0, 512]], dtype=np.int32)
+    _, with_rows = B.paged_decode_plan(nb, 64, 8, 128, mb, lens, shared, 152)
+    plan, _ = B.paged_decode_plan(nb, 64, 8, 128, mb, lens, shared, 152)
+    rows, tiles, _, _ = decode_plan(plan, with_rows, nb, 64, 8)
+    assert with_rows.n_row_items > 0
+    assert sorted(set((tiles[:, 5] - tiles[:, 4]).tolist())) == [256]
+    # the whole table shared: no split-KV item at all
+    full = np.array([[0, nb, 0, 600]], dtype=np.int32)
+    plan2, only_tiles = B.paged_decode_plan(nb, 64, 8, 128, mb, lens, full, 152)
+    _, tiles2, _, _ = decode_plan(plan2, only_tiles, nb, 64, 8)
+    assert only_tiles.n_row_items == 0
+    assert (tiles2[:, 5] - tiles2[:, 4]).max() < 256
+    assert only_tiles.n_tile_items >= 2 * 152
