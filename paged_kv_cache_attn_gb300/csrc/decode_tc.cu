@@ -292,55 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_after_sync();
       const uint32_t srow = lane_base + b * kT;
       const int valid = min(kT, (it.blk_end - (it.blk_begin + j * kTB)) * 16);
-      // Pass 1: row maximum over the tile's valid tokens.
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-      for (int c = 0; c < kT / 32; ++c) {
-        uint32_t sv[32];
-        tmem_ld32(srow + c * 32, sv);
-        tmem_wait_ld();
-        if (valid >= (c + 1) * 32) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sv[i]));
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i < valid)
-              mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sv[i]));
-        }
-      }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      const float m_tile = mx * p.scale_log2;
-      const bool need = m_tile > m_used + kRescale;
-      const float m_new = need ? m_tile : m_used;
-      const float alpha = need ? ex2(m_used - m_new) : 1.f;
-      l *= alpha;
-      m_used = m_new;
-      // Pass 2: P = 2^(s * scale_log2 - m) as bf16 pairs, written over the
-      // first 64 columns of this tile's own S buffer: chunk c of P lands on
-      // columns 16c .. 16c + 15, which this thread has already read.
-      const float neg_m = -m_used;
-#pragma unroll
-      for (int c = 0; c < kT / 32; ++c) {
-        uint32_t sv[32];
-        tmem_ld32(srow + c * 32, sv);
-        tmem_wait_ld();
-        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int t0 = c * 32 + 2 * i;
-          float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), p.scale_log2, neg_m));
-          float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), p.scale_log2, neg_m));
-          p0 = t0 < valid ? p0 : 0.f;
-          p1 = t0 + 1 < valid ? p1 : 0.f;
-          acc4[i & 3] += p0 + p1;
-          pk[i] = pack_bf16(p0, p1);
-        }
-        l += (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
-        tmem_st16(srow + c * 16, pk);
-      }
+      float alpha;
+      const bool need =
+          softmax_tile(srow, valid, p.scale_log2, kRescale, m_used, l, alpha);
       if (__any_sync(0xffffffffu, need) && j > 0) {
         // Rescale this row of O (it holds PV up to tile j - 1) once PV(j - 1)
         // is done.  PV(j) cannot have started (it waits for this tile's P),
@@ -351,16 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         fence_after_sync();
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(lane_base + kColO + c * 32, ov);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st32(lane_base + kColO + c * 32, ov);
-        }
+        rescale_o_row(lane_base + kColO, alpha);
       }
       tmem_wait_st();
       fence_before_sync();
@@ -377,21 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tcgen05.ld is warp-collective: decide once per warp.
     if (__all_sync(0xffffffffu,
                    done && ok && !*(volatile int*)&abort_sh)) {
-      float* dst = p.o + (int64_t)(it.prow_base + r) * 128;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(lane_base + kColO + c * 32, ov);
-        tmem_wait_ld();
-        if (r < it.nrows) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(dst + c * 32 + i) =
-                make_float4(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1]),
-                            __uint_as_float(ov[i + 2]),
-                            __uint_as_float(ov[i + 3]));
-        }
-      }
+      store_o_row(lane_base + kColO, p.o + (int64_t)(it.prow_base + r) * 128,
+                  r < it.nrows);
       if (r < it.nrows) p.ml[it.prow_base + r] = make_float2(m_used, l);
     }
   }

@@ -48,12 +48,11 @@ namespace tcw {
 using tc::fence_after_sync;
 using tc::fence_before_sync;
 using tc::idesc;
+using tc::rescale_o_row;
 using tc::sdesc;
+using tc::softmax_tile;
+using tc::store_o_row;
 using tc::tma_load_5d;
-using tc::tmem_ld32;
-using tc::tmem_st16;
-using tc::tmem_st32;
-using tc::tmem_wait_ld;
 using tc::tmem_wait_st;
 using tc::umma_commit;
 using tc::umma_ss;
@@ -329,68 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_after_sync();
       const int valid = min(kT, (it.blk_end - (it.blk_begin + j * kTB)) * 16);
-      // Pass 1: row maximum over the tile's valid tokens.
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-      for (int c = 0; c < kT / 32; ++c) {
-        uint32_t sv[32];
-        tmem_ld32(srow + c * 32, sv);
-        tmem_wait_ld();
-        if (valid >= (c + 1) * 32) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sv[i]));
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i < valid)
-              mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sv[i]));
-        }
-      }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      const float m_tile = mx * p.scale_log2;
-      const bool need = m_tile > m_used + kRescale;
-      const float m_new = need ? m_tile : m_used;
-      const float alpha = need ? ex2(m_used - m_new) : 1.f;
-      l *= alpha;
-      m_used = m_new;
-      // Pass 2: P = 2^(s * scale_log2 - m) as bf16 pairs over the first 64
-      // columns of S_m: chunk c of P lands on columns 16c .. 16c + 15, which
-      // this thread has already read.
-      const float neg_m = -m_used;
-#pragma unroll
-      for (int c = 0; c < kT / 32; ++c) {
-        uint32_t sv[32];
-        tmem_ld32(srow + c * 32, sv);
-        tmem_wait_ld();
-        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int t0 = c * 32 + 2 * i;
-          float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), p.scale_log2, neg_m));
-          float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), p.scale_log2, neg_m));
-          p0 = t0 < valid ? p0 : 0.f;
-          p1 = t0 + 1 < valid ? p1 : 0.f;
-          acc4[i & 3] += p0 + p1;
-          pk[i] = pack_bf16(p0, p1);
-        }
-        l += (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
-        tmem_st16(srow + c * 16, pk);
-      }
+      float alpha;
+      const bool need =
+          softmax_tile(srow, valid, p.scale_log2, kRescale, m_used, l, alpha);
       // O_m holds PV up to tile j - 1, all of it done (see the header).
-      if (__any_sync(0xffffffffu, need) && j > 0) {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(orow + c * 32, ov);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st32(orow + c * 32, ov);
-        }
-      }
+      if (__any_sync(0xffffffffu, need) && j > 0) rescale_o_row(orow, alpha);
       tmem_wait_st();
       fence_before_sync();
       __syncwarp();
@@ -407,21 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = m * 128 + r;
     if (m < n_m &&
         __all_sync(0xffffffffu, done && ok && !*(volatile int*)&abort_sh)) {
-      float* dst = p.o + (int64_t)(it.prow_base + row) * 128;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(orow + c * 32, ov);
-        tmem_wait_ld();
-        if (row < it.nrows) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(dst + c * 32 + i) =
-                make_float4(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1]),
-                            __uint_as_float(ov[i + 2]),
-                            __uint_as_float(ov[i + 3]));
-        }
-      }
+      store_o_row(orow, p.o + (int64_t)(it.prow_base + row) * 128,
+                  row < it.nrows);
       if (row < it.nrows) p.ml[it.prow_base + row] = make_float2(m_used, l);
     }
   }

@@ -148,5 +148,104 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a,
                : "memory");
 }
 
+// ---- the softmax rows of the tcgen05 tile kernels ---------------------------
+// One thread owns one query row (its TMEM lane).  S of a 128-token tile sits
+// in 128 fp32 columns at `srow`; `valid` of its tokens count.
+
+// Base-2 online softmax over one tile, with a lazy maximum: the row's
+// reference m moves (and O, l are rescaled by the returned alpha) only when
+// the tile's maximum exceeds it by more than `lazy` (log2 units), so every
+// weight stays below 2^lazy.  P = 2^(s * scale_log2 - m) is written as bf16
+// pairs over the first 64 columns of the same S: chunk c of P lands on
+// columns 16c .. 16c + 15, which this thread has already read.  Returns
+// whether m moved.
+__device__ __forceinline__ bool softmax_tile(uint32_t srow, int valid,
+                                             float scale_log2, float lazy,
+                                             float& m_used, float& l,
+                                             float& alpha) {
+  // Pass 1: row maximum over the tile's valid tokens.
+  float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t sv[32];
+    tmem_ld32(srow + c * 32, sv);
+    tmem_wait_ld();
+    if (valid >= (c + 1) * 32) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sv[i]));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (c * 32 + i < valid)
+          mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sv[i]));
+    }
+  }
+  const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+  const float m_tile = mx * scale_log2;
+  const bool need = m_tile > m_used + lazy;
+  const float m_new = need ? m_tile : m_used;
+  alpha = need ? ex2(m_used - m_new) : 1.f;
+  l *= alpha;
+  m_used = m_new;
+  // Pass 2: P, and its sum into l.
+  const float neg_m = -m_used;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t sv[32];
+    tmem_ld32(srow + c * 32, sv);
+    tmem_wait_ld();
+    float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int t0 = c * 32 + 2 * i;
+      float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), scale_log2, neg_m));
+      float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), scale_log2, neg_m));
+      p0 = t0 < valid ? p0 : 0.f;
+      p1 = t0 + 1 < valid ? p1 : 0.f;
+      acc4[i & 3] += p0 + p1;
+      pk[i] = pack_bf16(p0, p1);
+    }
+    l += (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+    tmem_st16(srow + c * 16, pk);
+  }
+  return need;
+}
+
+// This thread's row of O (128 fp32 columns at `orow`) times alpha.
+__device__ __forceinline__ void rescale_o_row(uint32_t orow, float alpha) {
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t ov[32];
+    tmem_ld32(orow + c * 32, ov);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+    tmem_st32(orow + c * 32, ov);
+  }
+}
+
+// The row's unnormalised partial result: O (128 fp32 columns at `orow`) to
+// dst (skipped for a row past the item's rows; the TMEM loads are
+// warp-collective, so every lane of the warp calls this).
+__device__ __forceinline__ void store_o_row(uint32_t orow, float* dst,
+                                            bool row_valid) {
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t ov[32];
+    tmem_ld32(orow + c * 32, ov);
+    tmem_wait_ld();
+    if (row_valid) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(dst + c * 32 + i) =
+            make_float4(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1]),
+                        __uint_as_float(ov[i + 2]), __uint_as_float(ov[i + 3]));
+    }
+  }
+}
+
 }  // namespace tc
 }  // namespace pkv
