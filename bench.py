@@ -314,7 +314,7 @@ def tile_kernel_name(info):
     return "+".join(names)
 
 
-def time_steps(bt, q, out, K, warmup, flush=None, before=None):
+def time_steps(bt, q, out, K, warmup, flush=None, before=None, after=None):
     """Time K decode steps after `warmup` untimed ones.  Returns (ms per step,
     per-kernel ms, per-step kernel events).
 
@@ -328,8 +328,8 @@ def time_steps(bt, q, out, K, warmup, flush=None, before=None):
     evicts the step's KV from L2, the read then evicts the written lines, so
     that the step neither finds the previous one's KV in L2 nor pays for the
     flush's write-backs -- and each step is timed by its own pair of events.
-    `before` (optional) runs right before the first timed pass, after the
-    warm-up (the ranks' barrier)."""
+    `before` / `after` (optional) run right before and right after the first
+    pass, with the device synchronised on both sides (the ranks' barriers)."""
     import torch
     from paged_kv_cache_attn_gb300 import binding as B
     stream = torch.cuda.current_stream()
@@ -372,6 +372,8 @@ def time_steps(bt, q, out, K, warmup, flush=None, before=None):
     run(False)
     end.record(stream)
     torch.cuda.synchronize()
+    if after is not None:
+        after()
     if flush is None:
         ms = start.elapsed_time(end) / K
     else:
@@ -505,11 +507,10 @@ def run_ours(args):
     K = args.steps
     peak, peak_kind = measured_peaks()
     with ClockSampler(torch.cuda.current_device()) as clk:
-        ms_step, per_kernel, evs = time_steps(
-            bt, q, out, K, args.warmup,
-            before=torch.distributed.barrier if ws > 1 else None)
+        barrier = torch.distributed.barrier if ws > 1 else None
+        ms_step, per_kernel, evs = time_steps(bt, q, out, K, args.warmup,
+                                              before=barrier, after=barrier)
     if ws > 1:
-        torch.distributed.barrier()
         t = torch.tensor([ms_step], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms_step = float(t.item())
