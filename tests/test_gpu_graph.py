@@ -22,6 +22,11 @@ CASES = {
                                            fan=16, suffix_tokens=37),
     "deep_tree": lambda: W.deep_tree(root_tokens=300, depth=3, min_seg=5,
                                      max_seg=40),
+    # a 696-row root (128-row tiles) and depth-1 segments of 80-176 rows
+    # (256-row items beside 128-row ones): both tile kernels, on two side
+    # streams, inside the capture
+    "wide_tree": lambda: W.deep_tree(root_tokens=300, depth=3, branching=5,
+                                     min_seg=20, max_seg=50),
 }
 
 
@@ -34,6 +39,8 @@ def test_captured_step_replays(name, kv_dtype):
     nb = len(cache.decode_ids)
     bt = cache.batch().upload()
     assert bt.info.n_tile_items > 0 and bt.info.n_row_items > 0  # both passes
+    if name == "wide_tree" and kv_dtype == "bf16":
+        assert 0 < bt.info.n_tile_wide_items < bt.info.n_tile_items
     q = torch.empty((nb, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
     out = torch.empty_like(q)
     # Warm up outside the capture (first-use function attributes, streams).

@@ -60,6 +60,8 @@ SMALL = {
                                       Hkv=8),
     "fanout_256": lambda: W.fanout(n_roots=2, root_tokens=777, fan=64,
                                    min_suffix=1, max_suffix=90),
+    "wide_tree": lambda: W.deep_tree(root_tokens=300, depth=3, branching=5,
+                                     min_seg=20, max_seg=50),
     "gqa_2": lambda: W.independent(n_seqs=3, min_len=17, max_len=300, Hq=8,
                                    Hkv=4, d=64),
     "gqa_16": lambda: W.fanout(n_roots=1, root_tokens=64, fan=3,
