@@ -146,18 +146,28 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
   }
 
   // Split-KV items: up to 128 blocks, halved while there are fewer than two
-  // items per SM.  Tile items: up to 256 blocks.  A tile item carries several
-  // microseconds of fixed cost (TMEM, barriers, Q, the first loads, the
-  // epilogue) and holds a whole SM, so fewer, longer tile items pay: the
-  // split-KV pass streams on the SMs they leave free (measured on the
-  // fan-out tree: 256 tile items of 32 blocks 0.238 ms, 64 of 128 blocks
-  // 0.215 ms).  Only a step with no split-KV items at all halves them to
-  // fill the GPU.
+  // items per SM.  A tile item carries several microseconds of fixed cost
+  // (TMEM, barriers, Q, the first loads, the epilogue and its 128 partial
+  // rows per kv-head) and holds a whole SM, so tile items are made as long
+  // as the step allows: up to the step's block work per SM (every item,
+  // tile or split, moves its blocks into one SM), with the split-KV pass
+  // streaming on the SMs they leave free.  Measured: the fan-out tree with
+  // 256 tile items of 32 blocks 0.238 ms, 64 of 128 blocks 0.215 ms; the
+  // long-context tree with tile items of 256, 512, 1024 and 2048 blocks
+  // 1.037, 1.010, 0.996 and 0.987 ms.  A step with no split-KV item at all
+  // halves its tile items until there are two per SM.
+  int64_t block_work = 0;
   bool any_rows = false;
-  for (const Unit& u : units) any_rows |= !u.tile;
+  for (const Unit& u : units) {
+    any_rows |= !u.tile;
+    block_work += (int64_t)(u.blk_end - u.blk_begin) *
+                  ceil_div(u.rows, rows_per(u)) * Hkv;
+  }
   const int32_t chunk_rows = pick_chunk(units, false, Hkv, num_sms, 128);
   const int32_t chunk_tile =
-      any_rows ? 256 : pick_chunk(units, true, Hkv, num_sms, 256);
+      any_rows ? (int32_t)std::min<int64_t>(
+                     INT32_MAX, std::max<int64_t>(8, block_work / num_sms))
+               : pick_chunk(units, true, Hkv, num_sms, 256);
 
   // Longest units first: their items come first, so the last wave of each
   // kernel is made of the short ones.  (Items of one unit have equal length

@@ -8,7 +8,7 @@ Each tree has 20 branches x 8 q-heads per kv-head = 160 rows: in bf16 one
 128-row tiles, the second one ragged), in e4m3 two 128-row tiles; the
 branches' own suffixes go to the split-KV pass.  The plan is made for one SM
 (the split sizes do not change the result), so that each tile item covers
-its whole segment (up to 256 blocks) instead of a short chunk of it.
+its whole segment instead of a chunk of it.
 """
 
 import numpy as np
@@ -43,9 +43,10 @@ def test_segment_lengths_at_ring_edges(blocks, kv_dtype):
     q = w.queries(len(cache.decode_ids))
     bt = cache.batch(num_sms=1,
                      flags=B.KV_PLAN_NARROW_TILES if narrow else 0).upload()
-    # every tile item covers the whole segment, or half of it past 256 blocks
+    # planned for one SM, every tile item covers its whole segment (the
+    # 325-block one in a single item of 40 tiles and a ragged tail)
     per_head = 1 if kv_dtype == "bf16" and not narrow else 2
-    assert bt.info.n_tile_items == 8 * per_head * (2 if blocks > 256 else 1)
+    assert bt.info.n_tile_items == 8 * per_head
     assert bt.info.n_tile_wide_items == (bt.info.n_tile_items
                                          if per_head == 1 else 0)
     qd = torch.from_numpy(q.view(np.int16)).cuda().view(torch.bfloat16)

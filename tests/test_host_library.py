@@ -418,23 +418,30 @@ def test_batched_append_is_all_or_nothing():
     B.kv_pool_destroy(h)
 
 
-def test_tile_items_stay_long_when_the_step_has_split_items():
-    """Tile items span 256 blocks (or the whole segment) whenever the step
-    also has split-KV items, however few SMs would be busy; a step made of
-    segments only halves them until there are two items per SM."""
-    nb, mb = 16, 600
+def test_tile_items_as_long_as_the_step_allows():
+    """With split-KV items in the step, a segment's tile items are as long as
+    the step's block work per SM (every tile and split item moves its blocks
+    into one SM), cut evenly; a step made of segments only halves them from
+    256 blocks until there are two items per SM."""
+    nb, mb, sms = 16, 600, 152
     lens = np.full(nb, 600 * 16, dtype=np.int32)
-    # 16 branches x 8 q-heads = 128 rows sharing 512 full blocks
-    shared = np.array([[0, nb, 0, 512]], dtype=np.int32)
-    _, with_rows = B.paged_decode_plan(nb, 64, 8, 128, mb, lens, shared, 152)
-    plan, _ = B.paged_decode_plan(nb, 64, 8, 128, mb, lens, shared, 152)
-    rows, tiles, _, _ = decode_plan(plan, with_rows, nb, 64, 8)
-    assert with_rows.n_row_items > 0
-    assert sorted(set((tiles[:, 5] - tiles[:, 4]).tolist())) == [256]
+    for seg in (512, 64):
+        # 16 branches x 8 q-heads = 128 rows (one 128-row tile) sharing `seg`
+        # full blocks; each branch keeps 600 - seg blocks of its own.
+        shared = np.array([[0, nb, 0, seg]], dtype=np.int32)
+        plan, info = B.paged_decode_plan(nb, 64, 8, 128, mb, lens, shared, sms)
+        rows, tiles, _, _ = decode_plan(plan, info, nb, 64, 8)
+        assert info.n_row_items > 0
+        work = seg * 8 + nb * (600 - seg) * 8          # block work of all items
+        chunk = max(8, work // sms)
+        pieces = -(-seg // chunk)
+        span = (tiles[:, 5] - tiles[:, 4]).tolist()
+        assert len(span) == pieces * 8
+        assert set(span) <= {seg // pieces, -(-seg // pieces)}
     # the whole table shared: no split-KV item at all
     full = np.array([[0, nb, 0, 600]], dtype=np.int32)
-    plan2, only_tiles = B.paged_decode_plan(nb, 64, 8, 128, mb, lens, full, 152)
+    plan2, only_tiles = B.paged_decode_plan(nb, 64, 8, 128, mb, lens, full, sms)
     _, tiles2, _, _ = decode_plan(plan2, only_tiles, nb, 64, 8)
     assert only_tiles.n_row_items == 0
     assert (tiles2[:, 5] - tiles2[:, 4]).max() < 256
-    assert only_tiles.n_tile_items >= 2 * 152
+    assert only_tiles.n_tile_items >= 2 * sms
