@@ -752,12 +752,41 @@ def run_ours(args):
                 torch.cuda.synchronize()
                 t_sp.append(e0.elapsed_time(e1))
                 t_re.append(e1.elapsed_time(e2))
+            # The link's own ceiling: one contiguous copy-engine copy of the
+            # same pinned buffer each way (scattered blocks cannot beat it).
+            dk = torch.empty_like(hk, device=dev)
+            t_h2d, t_d2h = [], []
+            for _ in range(3):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e2 = torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                e0.record(stream)
+                dk.copy_(hk, non_blocking=True)
+                e1.record(stream)
+                hk.copy_(dk, non_blocking=True)
+                e2.record(stream)
+                torch.cuda.synchronize()
+                t_h2d.append(e0.elapsed_time(e1))
+                t_d2h.append(e1.elapsed_time(e2))
+            del dk
+            half = hk.numel() * hk.element_size()
+            spill = byts / (min(t_sp) / 1e3) / 1e9
+            restore = byts / (min(t_re) / 1e3) / 1e9
+            link_d2h = half / (min(t_d2h) / 1e3) / 1e9
+            link_h2d = half / (min(t_h2d) / 1e3) / 1e9
             offload = {
                 "branches": len(victims), "blocks": nblk, "bytes": byts,
-                "spill_gbs": round(byts / (min(t_sp) / 1e3) / 1e9, 1),
-                "restore_gbs": round(byts / (min(t_re) / 1e3) / 1e9, 1),
+                "spill_gbs": round(spill, 1),
+                "restore_gbs": round(restore, 1),
+                "link_d2h_gbs": round(link_d2h, 1),
+                "link_h2d_gbs": round(link_h2d, 1),
+                "spill_frac_of_link": round(spill / link_d2h, 3),
+                "restore_frac_of_link": round(restore / link_h2d, 3),
                 "note": "one copy kernel per direction, device pool <-> "
-                        "pinned host memory; best of 3",
+                        "pinned host memory; best of 3.  link_*: a "
+                        "contiguous copy-engine copy of the pinned K buffer "
+                        "each way, the CPU-GPU link's ceiling",
             }
 
     # The same step captured once into a CUDA graph and replayed: what an

@@ -238,6 +238,16 @@ extern "C" kv_status paged_decode_plan(int32_t nb, int32_t Hq, int32_t Hkv,
       row_items.begin(), row_items.end(), [](const pkv::WorkItem& it) {
         return it.blk_end - it.blk_begin > pkv::kWarpItemBlocks;
       });
+  // Within each part, longest items first (stable: the items of one unit
+  // and chunk keep their order).  The hardware hands CTAs out in list order,
+  // so this is longest-processing-time-first scheduling: the last items to
+  // start are the shortest, and the pass's tail shrinks.  Items of one unit
+  // differ by at most a block, so the unit order above only approximates it.
+  const auto longer = [](const pkv::WorkItem& x, const pkv::WorkItem& y) {
+    return x.blk_end - x.blk_begin > y.blk_end - y.blk_begin;
+  };
+  std::stable_sort(row_items.begin(), first_short, longer);
+  std::stable_sort(first_short, row_items.end(), longer);
   int32_t n_warp_items = (int32_t)(row_items.end() - first_short);
   if (n_warp_items <= 2 * pkv::kSplitCtasPerSm * num_sms) n_warp_items = 0;
   // The 256-row tile items go first in the tile list.
