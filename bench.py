@@ -210,6 +210,8 @@ def traffic_per_launch(kernel, workload):
     if not d:
         return None
     src = os.path.join(ROOT, "paged_kv_cache_attn_gb300", "csrc", d["source"])
+    if not os.path.exists(src):
+        return None
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     return d["dram_bytes_per_launch"] if sha == d["source_sha"] else None
 
@@ -225,7 +227,8 @@ def measured_sharing(workload):
     d = json.load(open(p))
     for src, sha in d["sources"].items():
         f = os.path.join(ROOT, "paged_kv_cache_attn_gb300", "csrc", src)
-        if hashlib.sha256(open(f, "rb").read()).hexdigest()[:16] != sha:
+        if (not os.path.exists(f) or
+                hashlib.sha256(open(f, "rb").read()).hexdigest()[:16] != sha):
             return None
     e = d.get(workload) or d.get(workload + "_quarter")
     if not e:

@@ -64,7 +64,7 @@ __device__ __forceinline__ void q_ready_barrier() {
 
 struct Bars {
   uint64_t k_full[kNS], k_empty[kNS], v_full[kNS], v_empty[kNS], s_full[2],
-      p_full, pv_done, o_ready, drain;
+      p_full[2], pv_done, o_ready, drain;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -104,7 +104,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars.v_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&bars.s_full[b]), 1);
-    mbar_init(smem_u32(&bars.p_full), 4);
+    // P of tile j is reported on p_full[j % 2]: a softmax warp that runs a
+    // tile ahead arrives on the other barrier, so it cannot complete the
+    // phase PV(j) waits for before the slowest warp's P(j) is written.
+    for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&bars.p_full[b]), 4);
     mbar_init(smem_u32(&bars.pv_done), 1);
     mbar_init(smem_u32(&bars.o_ready), 1);
     mbar_init(smem_u32(&bars.drain), 1);
@@ -234,7 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       auto pv = [&](int jp) {
         const int s = jp % kNS;
-        if (!mbar_wait(smem_u32(&bars.p_full), jp & 1)) return false;
+        if (!mbar_wait(smem_u32(&bars.p_full[jp & 1]), (jp >> 1) & 1))
+          return false;
         if (!mbar_wait(smem_u32(&bars.v_full[s]), (jp / kNS) & 1)) return false;
         fence_after_sync();
         const uint32_t vst = sV + s * kKV;
@@ -267,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(smem_u32(&bars.s_full[b]));
         if (j >= 1) ok = pv(j - 1);
       }
-      if (ok) ok = pv(ntile - 1);
+      if (ok && ntile > 0) ok = pv(ntile - 1);
       if (!ok) {
         record_status(p.status, KV_ERR_TIMEOUT, 11);
         atomicExch(&abort_sh, 1);
@@ -285,7 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < ntile; ++j) {
       const int b = j & 1;
-      if (!mbar_wait(smem_u32(&bars.s_full[b]), (j >> 1) & 1)) {
+      // Warp-uniform: the TMEM accesses below are warp-collective.
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(smem_u32(&bars.s_full[b]), (j >> 1) & 1))) {
         ok = false;
         break;
       }
@@ -300,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // is done.  PV(j) cannot have started (it waits for this tile's P),
         // so the barrier has completed j - 1 or j phases and the parity wait
         // is exact.
-        if (!mbar_wait(smem_u32(&bars.pv_done), (j - 1) & 1)) {
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(smem_u32(&bars.pv_done), (j - 1) & 1))) {
           ok = false;
           break;
         }
@@ -310,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars.p_full));
+      if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[b]));
     }
     if (!ok) {
       if (lane == 0) record_status(p.status, KV_ERR_TIMEOUT, 12);

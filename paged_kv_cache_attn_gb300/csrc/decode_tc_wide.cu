@@ -322,7 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < ntile && m < n_m; ++j) {
-      if (!mbar_wait(smem_u32(&bars.s_full[m]), j & 1)) {
+      // Warp-uniform: the TMEM accesses below are warp-collective.
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(smem_u32(&bars.s_full[m]), j & 1))) {
         ok = false;
         break;
       }
