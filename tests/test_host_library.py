@@ -306,20 +306,34 @@ def test_plan_covers_every_token_once(name, flags):
     assert nw == (n_short if n_short > 2 * 3 * 152 else 0)
 
 
-def test_short_split_items_keep_their_order():
-    """The short items are moved behind the long ones without reordering
-    either group (a stable partition), and every item is still there."""
-    w = W.make("deep_tree")
+@pytest.mark.parametrize("name", ["deep_tree", "independent", "fanout"])
+def test_split_items_longest_first(name):
+    """The short items are moved behind the long ones, and within each group
+    the items run longest first (the hardware hands out CTAs in list order:
+    longest-processing-time-first scheduling).  Among items of equal length
+    the order of generation is kept (a stable sort), and every item is still
+    there."""
+    w = W.make(name)
     bt = H.Cache(w, with_data=False).batch(num_sms=152)
     rows, _, _, _ = decode_plan(bt.plan, bt.info, bt.nb, w.Hq, w.Hkv)
-    nw = bt.info.n_row_warp_items
-    assert nw > 1000                       # most deep_tree items are short
-    # Partial-row bases were handed out in generation order, so each group
-    # must still be in increasing base order.
+    span = rows[:, 5] - rows[:, 4]
+    short = span <= 16
+    n_short = int(short.sum())
+    groups = (slice(0, len(rows) - n_short), slice(len(rows) - n_short, None))
+    if name == "deep_tree":
+        assert bt.info.n_row_warp_items > 1000   # most items are short
+    # Partial-row bases were handed out in generation order.
     base = rows[:, 6]
-    assert (np.diff(base[:len(rows) - nw]) > 0).all()
-    assert (np.diff(base[len(rows) - nw:]) > 0).all()
+    for g in groups:
+        sp, b = span[g], base[g]
+        assert (np.diff(sp) <= 0).all()          # longest first
+        same = np.diff(sp) == 0
+        assert (np.diff(b)[same] > 0).all()      # stable among equal lengths
     assert sorted(base.tolist()) == sorted(set(base.tolist()))
+    if name == "independent":
+        # units of more than 128 blocks are cut into shorter items, so the
+        # generation order was not longest first: the sort moved items
+        assert (np.diff(base[groups[0]]) < 0).any()
 
 
 @pytest.mark.parametrize("fan,flags,want", [
