@@ -83,26 +83,45 @@ struct MoveArgs {
   int dst[kMaxDst / 2];
 };
 
+// U independent vectors per thread and iteration (all loaded, then
+// stored), so that U copies per thread are in flight over the CPU-GPU link.
+template <int U>
 __global__ void block_move_kernel(const __grid_constant__ MoveArgs a) {
   const int per_layer = 2 * a.kv_vecs + a.s_vecs;
   const int64_t per_pair = (int64_t)a.L * per_layer;
   const int64_t total = per_pair * a.n;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int pair = (int)(i / per_pair);
-    const int64_t r = i - pair * per_pair;
-    const int64_t layer = r / per_layer;
-    int vec = (int)(r - layer * per_layer);
-    const int64_t fb = layer * a.from_blocks + a.src[pair];
-    const int64_t tb = layer * a.to_blocks + a.dst[pair];
-    if (vec < a.kv_vecs) {
-      a.to_k[tb * a.kv_vecs + vec] = a.from_k[fb * a.kv_vecs + vec];
-    } else if ((vec -= a.kv_vecs) < a.kv_vecs) {
-      a.to_v[tb * a.kv_vecs + vec] = a.from_v[fb * a.kv_vecs + vec];
-    } else {
-      vec -= a.kv_vecs;
-      a.to_s[tb * a.s_vecs + vec] = a.from_s[fb * a.s_vecs + vec];
+  const int64_t step = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i0 < total;
+       i0 += step * U) {
+    uint4 v[U];
+    uint4* d[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + u * step;
+      d[u] = nullptr;
+      if (i < total) {
+        const int pair = (int)(i / per_pair);
+        const int64_t r = i - pair * per_pair;
+        const int64_t layer = r / per_layer;
+        int vec = (int)(r - layer * per_layer);
+        const int64_t fb = layer * a.from_blocks + a.src[pair];
+        const int64_t tb = layer * a.to_blocks + a.dst[pair];
+        if (vec < a.kv_vecs) {
+          v[u] = a.from_k[fb * a.kv_vecs + vec];
+          d[u] = a.to_k + tb * a.kv_vecs + vec;
+        } else if ((vec -= a.kv_vecs) < a.kv_vecs) {
+          v[u] = a.from_v[fb * a.kv_vecs + vec];
+          d[u] = a.to_v + tb * a.kv_vecs + vec;
+        } else {
+          vec -= a.kv_vecs;
+          v[u] = a.from_s[fb * a.s_vecs + vec];
+          d[u] = a.to_s + tb * a.s_vecs + vec;
+        }
+      }
     }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (d[u]) *d[u] = v[u];
   }
 }
 
@@ -270,6 +289,16 @@ int launch_block_move(const PoolBufs& from, const PoolBufs& to, int L,
   a.L = L;
   a.kv_vecs = (int)(kv_bytes / 16);
   a.s_vecs = (int)(s_bytes / 16);
+  // A light grid: one CTA for every four SMs, four 16-byte vectors in
+  // flight per thread.  The moves that cross the CPU-GPU link (spill,
+  // restore) need no more to run at the link's speed (restore 205 GB/s of
+  // its 211).  A restore is also a prefetch that runs beside decode steps,
+  // and the decode steps pay for the copy's footprint on the SMs: beside a
+  // restore they took 37% longer with a grid filling every SM's thread
+  // slots, 11% with a CTA per SM and 4% with this one.
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   for (int i0 = 0; i0 < n; i0 += kMaxDst / 2) {
     a.n = std::min(n - i0, kMaxDst / 2);
     for (int i = 0; i < a.n; ++i) {
@@ -277,7 +306,9 @@ int launch_block_move(const PoolBufs& from, const PoolBufs& to, int L,
       a.dst[i] = dst[i0 + i];
     }
     const int64_t work = (int64_t)a.n * L * (2 * a.kv_vecs + a.s_vecs);
-    block_move_kernel<<<grid_for(work), 256, 0, (cudaStream_t)stream>>>(a);
+    const int grid = (int)std::min<int64_t>(std::max(sms / 4, 1),
+                                            std::max<int64_t>(1, (work + 255) / 256));
+    block_move_kernel<4><<<grid, 256, 0, (cudaStream_t)stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
   }

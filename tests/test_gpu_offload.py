@@ -76,3 +76,56 @@ def test_spill_restore_round_trip():
         err = np.abs(gpu[b] - want[b])
         assert (err <= 2e-3 + 1e-2 * np.abs(want[b])).all()
     cache.close()
+
+
+def test_restore_as_prefetch_beside_decode():
+    """Spilled branches come back on a side stream while the step keeps
+    decoding the branches still resident (a prefetch: the restore pops device
+    blocks that no batch built before it references).  Both the steps that
+    run beside the restore and a step over every branch after it match the
+    oracle."""
+    w = W.fanout(n_roots=2, root_tokens=256, fan=8, min_suffix=1,
+                 max_suffix=100)
+    w.num_blocks += 64
+    cache = H.Cache(w)
+    slots = 256
+    shape = (w.num_layers, slots, w.Hkv, w.block_size, w.d)
+    hk = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+    B.kv_offload_attach(cache.h, hk, hv, slots)
+    ids = cache.decode_ids
+    victims, others = ids[::2], ids[1::2]
+    assert B.kv_spill(cache.h, victims) > 0
+    torch.cuda.synchronize()
+    ref = rp.replay(w, with_data=False)
+    q = w.queries(len(ids))
+    # The resident branches' batch, built before the restore.
+    bo = cache.batch(ids=others).upload()
+    qo = torch.from_numpy(np.ascontiguousarray(q[1::2]).view(np.int16)).cuda() \
+        .view(torch.bfloat16)
+    outs = [torch.empty_like(qo) for _ in range(3)]
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    done = torch.cuda.Event()
+    with torch.cuda.stream(side):
+        assert B.kv_restore(cache.h, victims, stream=side) > 0
+        done.record(side)
+    for o in outs:                       # on the current stream, beside it
+        bo.decode(qo, o)
+    torch.cuda.current_stream().wait_event(done)
+    want = rp.decode_rows(ref, q, range(len(ids)), w.scale)
+    for o in outs:
+        gpu = att.bf16_to_f64(_bits(o))
+        for k in range(len(others)):
+            err = np.abs(gpu[k] - want[2 * k + 1])
+            assert (err <= 2e-3 + 1e-2 * np.abs(want[2 * k + 1])).all()
+    # Every branch, restored ones included, after the restore.
+    bt = cache.batch().upload()
+    qd = torch.from_numpy(q.view(np.int16)).cuda().view(torch.bfloat16)
+    out = torch.empty_like(qd)
+    bt.decode(qd, out)
+    gpu = att.bf16_to_f64(_bits(out))
+    for b in range(len(ids)):
+        err = np.abs(gpu[b] - want[b])
+        assert (err <= 2e-3 + 1e-2 * np.abs(want[b])).all()
+    cache.close()
