@@ -791,12 +791,14 @@ def run_ours(args):
                         "contiguous copy-engine copy of the pinned K buffer "
                         "each way, the CPU-GPU link's ceiling",
             }
-            # Prefetch: the spilled branches come back on a side stream while
-            # the step keeps decoding the branches that stayed resident (their
-            # batch is built before the restore and references none of the
-            # device blocks it pops).  As many steps as one restore takes.
-            gone = set(victims)
-            others = [i for i in cache.decode_ids if i not in gone]
+        # Prefetch: the spilled branches come back on a side stream while the
+        # step keeps decoding the branches that stayed resident (their batch
+        # is built before the restore and references none of the device
+        # blocks it pops).  As many steps as one restore takes.
+        gone = set(victims)
+        others = ([i for i in cache.decode_ids if i not in gone]
+                  if victims and nblk > 0 else [])
+        if others:
             B.kv_spill(cache.h, victims)
             torch.cuda.synchronize()
             bo = cache.batch(ids=others).upload()
