@@ -218,6 +218,10 @@ __global__ void __launch_bounds__(128, 3)
 
   bool timed_out = false;
   int k = 0;
+  // An item of at most 8 rows (one branch at G <= 8) leaves rows 8-15 of the
+  // 16-row MMA tile empty: their softmax is skipped (uniform in the warp),
+  // and their P is zero.
+  const bool lo_only = it.nrows <= 8;
   // Two of the warp's blocks per iteration (a and a + 1 of its sequence):
   // four independent QK accumulation chains and one softmax update over 32
   // tokens.  m_r is a lazy reference maximum: it moves (and O, l are
@@ -306,9 +310,10 @@ __global__ void __launch_bounds__(128, 3)
       vfac = vref / vmax;
       vref = vmax;
     }
-    float alpha[2];
+    float alpha[2] = {1.f, 1.f};
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
+      if (hr == 1 && lo_only) break;
       float mx = -INFINITY;
 #pragma unroll
       for (int u = 0; u < 2; ++u)
@@ -316,7 +321,6 @@ __global__ void __launch_bounds__(128, 3)
                              fmaxf(x[u][1][2 * hr], x[u][1][2 * hr + 1])));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      alpha[hr] = 1.f;
       if (mx > m_r[hr] + 8.f) {  // also when m_r is -inf and mx finite
         alpha[hr] = ex2(m_r[hr] - mx);
         m_r[hr] = mx;
@@ -342,6 +346,10 @@ __global__ void __launch_bounds__(128, 3)
       float pr[2][4];
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
+        if (hr == 1 && lo_only) {
+          pr[0][2] = pr[0][3] = pr[1][2] = pr[1][3] = 0.f;
+          break;
+        }
         const float m_use = m_r[hr] == -INFINITY ? 0.f : m_r[hr];
         float sum = 0.f;
 #pragma unroll
